@@ -1,0 +1,318 @@
+// fp8q.cu -- libfp8q.so: the C ABI declared in include/fp8q.h.
+//
+// Host side only validates arguments, builds TMA tensor maps and launches
+// the kernels of quantize.cuh / gemm.cuh on the caller's stream.  It never
+// allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fp8q.h"
+#include "gemm.cuh"
+#include "quantize.cuh"
+
+namespace {
+
+using namespace fp8q;
+
+constexpr int kVersion = 100;  // 0.1.0
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+};
+
+// Per-device facts, probed once per device.
+DeviceInfo device_info(int dev) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool probed[64] = {};
+  if (dev < 0 || dev >= 64) return DeviceInfo{};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!probed[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+      cache[dev].ok = (major == 10 && minor == 3);
+      cache[dev].sms = sms;
+    }
+    probed[dev] = true;
+  }
+  return cache[dev];
+}
+
+int check_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8Q_ERR_CUDA;
+  DeviceInfo di = device_info(dev);
+  if (!di.ok) return FP8Q_ERR_DEVICE;
+  if (out) *out = di;
+  return FP8Q_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 tensor [rows][cols] (cols contiguous), box 128 bytes x box_rows,
+// 128-byte swizzle.  Out-of-range elements of a box read as zero.
+bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA; }
+
+template <bool kF32, int kMode>
+int launch_quant(const QuantArgs& a, int64_t grid_x, int64_t grid_y, cudaStream_t stream) {
+  if (grid_y > 65535) return FP8Q_ERR_SHAPE;
+  quant_tile_kernel<kF32, kMode><<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(grid_y)), 128, 0,
+                                   stream>>>(a);
+  return launch_status();
+}
+
+template <int kMode>
+int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cudaStream_t s) {
+  return in_dtype == FP8Q_FP32 ? launch_quant<true, kMode>(a, gx, gy, s) : launch_quant<false, kMode>(a, gx, gy, s);
+}
+
+template <bool kOutF32, int kSbGran, bool kGrouped>
+int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+  auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped>;
+  const uint32_t smem = kGrouped ? kSmemGrouped : kSmemDense;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, a);
+  return launch_status();
+}
+
+int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C, int64_t M,
+                int64_t N, int64_t K, int out_dtype, int sb_gran, const int32_t* row_offsets, int32_t E,
+                cudaStream_t stream) {
+  const bool grouped = row_offsets != nullptr;
+  if (out_dtype != FP8Q_BF16 && out_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (sb_gran != 128 && sb_gran != 1) return FP8Q_ERR_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (grouped && (E < 1 || E > kMaxExperts)) return FP8Q_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+    return FP8Q_ERR_SHAPE;
+  if (grouped && static_cast<int64_t>(E) * N > (int64_t(1) << 31) - 1) return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!Aq || !sA || !Bq || !sB || !C) return FP8Q_ERR_NULL;
+  if (!aligned16(Aq) || !aligned16(sA) || !aligned16(Bq) || !aligned16(sB) || !aligned16(C) ||
+      (grouped && !aligned16(row_offsets)))
+    return FP8Q_ERR_ALIGN;
+  DeviceInfo di;
+  int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, Aq, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM)) return FP8Q_ERR_CUDA;
+  const uint64_t brows = grouped ? static_cast<uint64_t>(E) * N : static_cast<uint64_t>(N);
+  if (!make_tmap_u8(&tb, Bq, static_cast<uint64_t>(K), brows, kBN)) return FP8Q_ERR_CUDA;
+
+  GemmArgs a;
+  a.sA = sA;
+  a.lds_a = M;
+  a.sB = sB;
+  a.C = C;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+  a.tiles_n = static_cast<int>((N + kBN - 1) / kBN);
+  a.row_offsets = row_offsets;
+  a.E = grouped ? E : 1;
+
+  int64_t tiles_upper;
+  if (grouped) {
+    tiles_upper = (static_cast<int64_t>(a.tiles_m) + E) * a.tiles_n;
+  } else {
+    tiles_upper = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
+  }
+  if (tiles_upper > (int64_t(1) << 31) - 1) return FP8Q_ERR_SHAPE;
+  const int grid = static_cast<int>(tiles_upper < di.sms ? tiles_upper : di.sms);
+  const bool f32 = out_dtype == FP8Q_FP32;
+  if (grouped) {
+    return f32 ? launch_gemm_t<true, 128, true>(ta, tb, a, grid, stream)
+               : launch_gemm_t<false, 128, true>(ta, tb, a, grid, stream);
+  }
+  if (sb_gran == 1) {
+    return f32 ? launch_gemm_t<true, 1, false>(ta, tb, a, grid, stream)
+               : launch_gemm_t<false, 1, false>(ta, tb, a, grid, stream);
+  }
+  return f32 ? launch_gemm_t<true, 128, false>(ta, tb, a, grid, stream)
+             : launch_gemm_t<false, 128, false>(ta, tb, a, grid, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8q_version(void) { return kVersion; }
+
+const char* fp8q_status_string(int status) {
+  switch (status) {
+    case FP8Q_OK: return "ok";
+    case FP8Q_ERR_NULL: return "null pointer argument";
+    case FP8Q_ERR_SHAPE: return "invalid shape (negative size or divisibility rule broken)";
+    case FP8Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FP8Q_ERR_DTYPE: return "unknown dtype or granularity code";
+    case FP8Q_ERR_DEVICE: return "current device is not sm_103 (B300)";
+    case FP8Q_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FP8Q_ERR_TIMEOUT: return "a kernel pipeline wait timed out on the device";
+    default: return "unknown status";
+  }
+}
+
+int fp8q_quantize_act(const void* x, int in_dtype, int64_t M, int64_t K, uint8_t* q_row, float* s_row,
+                      uint8_t* q_colT, float* s_col, fp8q_stream_t stream) {
+  const bool row = q_row != nullptr || s_row != nullptr;
+  const bool col = q_colT != nullptr || s_col != nullptr;
+  if (in_dtype != FP8Q_BF16 && in_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (M < 0 || K <= 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (col && M % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!x) return FP8Q_ERR_NULL;
+  if (!row && !col) return FP8Q_ERR_NULL;
+  if ((row && (!q_row || !s_row)) || (col && (!q_colT || !s_col))) return FP8Q_ERR_NULL;
+  if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(s_row))) ||
+      (col && (!aligned16(q_colT) || !aligned16(s_col))))
+    return FP8Q_ERR_ALIGN;
+  int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  QuantArgs a{};
+  a.x = x;
+  a.M = M;
+  a.K = K;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.ld_srow = M;
+  a.q_colT = q_colT;
+  a.s_col = s_col;
+  const int64_t gx = K / 128, gy = (M + 127) / 128;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (row && col) return launch_quant_dt<kQRow | kQCol>(in_dtype, a, gx, gy, s);
+  if (row) return launch_quant_dt<kQRow>(in_dtype, a, gx, gy, s);
+  return launch_quant_dt<kQCol>(in_dtype, a, gx, gy, s);
+}
+
+int fp8q_quantize_act_gather(const void* x, int in_dtype, int64_t M, int64_t K, const int32_t* src_rows, int64_t R,
+                             uint8_t* q_row, float* s_row, fp8q_stream_t stream) {
+  if (in_dtype != FP8Q_BF16 && in_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (M < 0 || R < 0 || K <= 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (R > 0 && M == 0) return FP8Q_ERR_SHAPE;
+  if (R == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!x || !src_rows || !q_row || !s_row) return FP8Q_ERR_NULL;
+  if (!aligned16(x) || !aligned16(src_rows) || !aligned16(q_row) || !aligned16(s_row)) return FP8Q_ERR_ALIGN;
+  int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  QuantArgs a{};
+  a.x = x;
+  a.M = R;
+  a.K = K;
+  a.src_rows = src_rows;
+  a.q_row = q_row;
+  a.s_row = s_row;
+  a.ld_srow = R;
+  return launch_quant_dt<kQRow>(in_dtype, a, K / 128, (R + 127) / 128, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_quantize_weight_ex(const void* w, int in_dtype, int64_t N, int64_t K, uint8_t* q, float* s, uint8_t* q_t,
+                            float* s_t, fp8q_stream_t stream) {
+  const bool fw = q != nullptr || s != nullptr;
+  const bool tr = q_t != nullptr || s_t != nullptr;
+  if (in_dtype != FP8Q_BF16 && in_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (N < 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (N == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!w) return FP8Q_ERR_NULL;
+  if (!fw && !tr) return FP8Q_ERR_NULL;
+  if ((fw && (!q || !s)) || (tr && (!q_t || !s_t))) return FP8Q_ERR_NULL;
+  if (!aligned16(w) || (fw && (!aligned16(q) || !aligned16(s))) || (tr && (!aligned16(q_t) || !aligned16(s_t))))
+    return FP8Q_ERR_ALIGN;
+  int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  QuantArgs a{};
+  a.x = w;
+  a.M = N;
+  a.K = K;
+  a.q_blk = q;
+  a.s_blk = s;
+  a.q_blkT = q_t;
+  a.s_blkT = s_t;
+  const int64_t gx = K / 128, gy = N / 128;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (fw && tr) return launch_quant_dt<kQBlk | kQBlkT>(in_dtype, a, gx, gy, cs);
+  if (fw) return launch_quant_dt<kQBlk>(in_dtype, a, gx, gy, cs);
+  return launch_quant_dt<kQBlkT>(in_dtype, a, gx, gy, cs);
+}
+
+int fp8q_quantize_weight(const void* w, int in_dtype, int64_t N, int64_t K, uint8_t* q, float* s,
+                         fp8q_stream_t stream) {
+  if (N != 0 && (!q || !s)) return FP8Q_ERR_NULL;
+  return fp8q_quantize_weight_ex(w, in_dtype, N, K, q, s, nullptr, nullptr, stream);
+}
+
+int fp8q_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C, int64_t M, int64_t N,
+              int64_t K, int out_dtype, fp8q_stream_t stream) {
+  return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, 128, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_gemm_ex(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C, int64_t M,
+                 int64_t N, int64_t K, int out_dtype, int sb_gran_n, fp8q_stream_t stream) {
+  return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_grouped_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C,
+                      const int32_t* row_offsets, int32_t E, int64_t total_rows, int64_t N, int64_t K, int out_dtype,
+                      fp8q_stream_t stream) {
+  if (!row_offsets && total_rows != 0) return FP8Q_ERR_NULL;
+  if (!row_offsets) return E < 1 || E > kMaxExperts ? FP8Q_ERR_SHAPE : FP8Q_OK;
+  return gemm_common(Aq, sA, Bq, sB, C, total_rows, N, K, out_dtype, 128, row_offsets, E,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_get_device_status(fp8q_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, fp8q::g_status_word, sizeof(v)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fp8q::g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FP8Q_ERR_CUDA;
+  }
+  return static_cast<int>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,359 @@
+// gemm.cuh -- block-scaled FP8 (E4M3) GEMM with FP32 promotion every 128 K,
+// dense and MoE-grouped, for sm_103a (tcgen05 + TMEM + TMA).
+//
+// The method: tensor cores accumulate each 128-element K interval with their
+// own limited internal precision; at the end of the interval the partial sum
+// is copied to FP32 registers on the CUDA cores, multiplied by the two
+// dequantization scales and added into a full-precision FP32 accumulator
+// ("Eliminate Deepseek Ai News For Good", the MMA-precision passage;
+// inprokorea.com page, the 128-element accumulation-interval passage;
+// "Is aI Hitting a Wall?", the dequantization passage).
+//
+// B300 design (the pages' Hopper ping-pong of two WGMMA warpgroups is prior
+// art, replaced by):
+//   warp 0       TMA producer: one 128x128 A tile + one 256x128 B tile per
+//                K-block into a kStages-deep ring of 128B-swizzled smem.
+//   warp 1       TMEM owner + single-thread MMA issuer: per K-block four
+//                tcgen05.mma.kind::f8f6f4 (128x256x32) into a FRESH TMEM
+//                partial (the first with accumulate off).  Two partial
+//                buffers (2 x 256 FP32 columns = all 512) alternate, so the
+//                MMAs of block kb+1 overlap the promotion of block kb.
+//   warps 4..11  promotion + epilogue: each thread owns one row and 128
+//                columns of the 128x256 tile in 128 FP32 registers; per
+//                K-block it tcgen05.ld's its slice of the partial, frees the
+//                buffer, and does acc = fma(P, sA*sB, acc).  At the end of
+//                a tile it rounds (BF16, RNE) or keeps FP32 and stores.
+// Warps 2-3 idle.  Registers: warpgroup 0 gives up all but 56 per thread
+// (setmaxnreg) so the two promotion warpgroups can hold 224 each: the
+// 384 x 168 registers of the launch are exactly 128 x 56 + 256 x 224.
+// The grid is persistent (one CTA per SM); tiles are striped over CTAs.
+// Every mbarrier wait is bounded (see mbar_wait): on expiry the kernel
+// records a timeout in the status word and unwinds without trapping.
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8q {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 384;
+constexpr uint32_t kRegsCtl = 56;    // warpgroup 0 after setmaxnreg.dec
+constexpr uint32_t kRegsMath = 224;  // warpgroups 1-2 after setmaxnreg.inc
+constexpr int kMaxExperts = 1024;
+constexpr uint32_t kABytes = kBM * kBK;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK;  // 32 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
+
+// dynamic shared memory layout (offsets from a 1024-aligned base)
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffBar = kOffB + kStages * kBBytes;       // 12 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;               // tmem base, abort flag
+constexpr uint32_t kOffPref = kOffMisc + 16;                  // grouped: tile prefix [E+1]
+constexpr uint32_t kOffRowOff = kOffPref + 4 * (kMaxExperts + 1);  // grouped: row offsets [E+1]
+constexpr uint32_t kSmemDense = kOffPref + 1024;              // + alignment slack
+constexpr uint32_t kSmemGrouped = kOffRowOff + 4 * (kMaxExperts + 1) + 1024;
+
+struct GemmArgs {
+  const float* sA;   // [K/128][lds_a]
+  int64_t lds_a;
+  const float* sB;   // gran 128: [E][N/128][K/128]; gran 1: [K/128][N]
+  void* C;           // [rows][N]
+  int64_t M;         // dense rows
+  int64_t N;
+  int64_t K;
+  int tiles_m;       // dense
+  int tiles_n;
+  const int32_t* row_offsets;  // grouped [E+1]
+  int E;
+};
+
+struct TileInfo {
+  int64_t m0;       // first row (global)
+  int64_t row_end;  // rows >= row_end are not this tile's
+  int64_t n0;       // first column
+  int32_t b_row;    // row coordinate of the B tile in the B tensor map
+  int64_t sb_off;   // expert offset into sB (grouped)
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs& a, const int* pref, const int* roff) {
+  TileInfo ti;
+  if constexpr (!kGrouped) {
+    const int mt = t % a.tiles_m;
+    const int nt = t / a.tiles_m;
+    ti.m0 = static_cast<int64_t>(mt) * kBM;
+    ti.row_end = a.M;
+    ti.n0 = static_cast<int64_t>(nt) * kBN;
+    ti.b_row = nt * kBN;
+    ti.sb_off = 0;
+  } else {
+    // expert e with pref[e] <= t < pref[e+1] (largest such e skips empties)
+    int lo = 0, hi = a.E;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pref[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int r0 = roff[e], r1 = roff[e + 1];
+    const int mtiles = (r1 - r0 + kBM - 1) / kBM;
+    const int local = t - pref[e];
+    const int nt = local / mtiles;  // all M-tiles of one N-slab run together
+    const int mt = local % mtiles;
+    ti.m0 = r0 + static_cast<int64_t>(mt) * kBM;
+    ti.row_end = r1 < a.M ? r1 : a.M;  // never past total_rows, even for bad offsets
+    ti.n0 = static_cast<int64_t>(nt) * kBN;
+    ti.b_row = static_cast<int32_t>(static_cast<int64_t>(e) * a.N + ti.n0);
+    ti.sb_off = static_cast<int64_t>(e) * (a.N / 128) * (a.K / 128);
+  }
+  return ti;
+}
+
+template <bool kOutF32, int kSbGran, bool kGrouped>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + kOffBar;            // [kStages]
+  const uint32_t bar_empty = bar_full + kStages * 8;    // [kStages]
+  const uint32_t bar_tfull = bar_empty + kStages * 8;   // [2]
+  const uint32_t bar_tempty = bar_tfull + 2 * 8;        // [2]
+  const uint32_t bar_drain = bar_tempty + 2 * 8;        // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* pref = reinterpret_cast<int*>(smem + kOffPref);
+  int* roff = reinterpret_cast<int*>(smem + kOffRowOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t KB = args.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 8);  // one arrive per promotion warp
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if constexpr (kGrouped) {
+    if (warp == 4) {
+      // tile prefix over experts: pref[e] = sum_{e' < e} ceil(rows_e'/128) * tiles_n
+      const int E = args.E;
+      const int per = (E + 31) / 32;
+      const int lo = lane * per;
+      const int hi = min(E, lo + per);
+      int local = 0;
+      for (int e = lo; e < hi; ++e) {
+        const int r0 = __ldg(args.row_offsets + e), r1 = __ldg(args.row_offsets + e + 1);
+        roff[e] = r0;
+        local += ((r1 - r0 + kBM - 1) / kBM) * args.tiles_n;
+      }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - local;
+      for (int e = lo; e < hi; ++e) {
+        pref[e] = run;
+        const int r0 = roff[e], r1 = __ldg(args.row_offsets + e + 1);
+        run += ((r1 - r0 + kBM - 1) / kBM) * args.tiles_n;
+      }
+      if (lane == 31) {
+        pref[E] = incl;
+        roff[E] = __ldg(args.row_offsets + E);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = kGrouped ? pref[args.E] : args.tiles_m * args.tiles_n;
+
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsCtl>();
+  }
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
+        for (int64_t kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_full + 8 * stage, kABytes + kBBytes);
+          tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, static_cast<int32_t>(kb * kBK),
+                      static_cast<int32_t>(ti.m0), bar_full + 8 * stage);
+          tma_load_2d(sbase + kOffB + stage * kBBytes, &tmB, static_cast<int32_t>(kb * kBK), ti.b_row,
+                      bar_full + 8 * stage);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for the copies this thread still has in flight
+        for (uint32_t i = 0; i < kStages && i < issued; ++i) {
+          if (stage == 0) { stage = kStages; phase ^= 1u; }
+          --stage;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar_full + 8 * stage, phase) && globaltimer_ns() - t0 < 1000000ull) {}
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_k_sw128(sbase + kOffA + stage * kABytes);
+          const uint64_t bdesc = smem_desc_k_sw128(sbase + kOffB + stage * kBBytes);
+          const uint32_t d = tmem_base + buf * kBN;
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            // K-slice k of the 128-byte swizzled rows: +32 bytes = +2 in the
+            // descriptor's 16-byte address units
+            mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+          }
+          any = true;
+          mma_commit(bar_empty + 8 * stage);
+          mma_commit(bar_tfull + 8 * buf);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          buf ^= 1u;
+          if (buf == 0) bphase ^= 1u;
+        }
+      }
+      if (!ok && any) {
+        // drain: wait (bounded) until every MMA this thread issued is done
+        mma_commit(bar_drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < 1000000ull) {}
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ promotion
+    setmaxnreg_inc<kRegsMath>();
+    const int q = warp & 3;         // TMEM lane quadrant this warp may access
+    const int h = (warp - 4) >> 2;  // column half of the tile: 0 or 1
+    const int row = q * 32 + lane;  // tile-local row
+    const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t buf = 0, bphase = 0;
+    bool ok = true;
+    const float* __restrict__ sA = args.sA;
+    const float* __restrict__ sB = args.sB;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
+      const int64_t m = ti.m0 + row;
+      const bool row_ok = m < ti.row_end;
+      const int64_t nh = ti.n0 + h * 128;  // first column of this thread's half
+      const bool cols_ok = nh < args.N;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        const float sa = row_ok ? __ldg(sA + kb * args.lds_a + m) : 0.f;
+        float sb = 0.f;
+        if constexpr (kSbGran == 128) {
+          if (cols_ok) sb = __ldg(sB + ti.sb_off + (nh >> 7) * KB + kb);
+        } else {
+          // warm L1 with the next K-block's per-column scales of this half
+          if (cols_ok && kb + 1 < KB) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(sB + (kb + 1) * args.N + nh + lane * 4));
+          }
+        }
+        if (!mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag)) { ok = false; break; }
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + t_lane + buf * kBN + h * 128;
+        const float scale = sa * sb;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t p[32];
+          tmem_ld_32x32b_x32(taddr + c4 * 32, p);
+          tmem_ld_wait();
+          if (c4 == 3) {
+            // the whole partial of this warp is in registers: free the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+          }
+          if constexpr (kSbGran == 128) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[c4 * 32 + j] = fmaf(__uint_as_float(p[j]), scale, acc[c4 * 32 + j]);
+          } else {
+            const float4* sbv = reinterpret_cast<const float4*>(sB + kb * args.N + nh + c4 * 32);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 b4 = cols_ok ? __ldg(sbv + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              acc[c4 * 32 + 4 * j4 + 0] = fmaf(__uint_as_float(p[4 * j4 + 0]) * b4.x, sa, acc[c4 * 32 + 4 * j4 + 0]);
+              acc[c4 * 32 + 4 * j4 + 1] = fmaf(__uint_as_float(p[4 * j4 + 1]) * b4.y, sa, acc[c4 * 32 + 4 * j4 + 1]);
+              acc[c4 * 32 + 4 * j4 + 2] = fmaf(__uint_as_float(p[4 * j4 + 2]) * b4.z, sa, acc[c4 * 32 + 4 * j4 + 2]);
+              acc[c4 * 32 + 4 * j4 + 3] = fmaf(__uint_as_float(p[4 * j4 + 3]) * b4.w, sa, acc[c4 * 32 + 4 * j4 + 3]);
+            }
+          }
+        }
+        buf ^= 1u;
+        if (buf == 0) bphase ^= 1u;
+      }
+      if (!ok) break;
+
+      // ---- epilogue: this thread's row, 128 columns ----
+      if (row_ok && cols_ok) {
+        if constexpr (kOutF32) {
+          float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.C) + m * args.N + nh);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            out[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        } else {
+          uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.N + nh);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            out[j] = make_uint4(cvt_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), cvt_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                                cvt_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), cvt_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace fp8q

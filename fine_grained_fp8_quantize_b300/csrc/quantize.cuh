@@ -1,0 +1,240 @@
+// quantize.cuh -- HBM-bound fine-grained E4M3 quantizers for sm_103a.
+//
+// One CTA (4 warps, 128 threads) owns one 128 x 128 tile of the input.
+// Thread (warp w, lane l) holds rows w*32 + (l/16)*16 + j (j = 0..15) and
+// columns (l%16)*8 .. +7 of the tile in registers, loaded with 16-byte
+// vector loads (a warp instruction reads two full 256-byte tile rows).
+// From those registers it forms, as the mode asks:
+//   ROW   1x128 groups (one row, 128 channels): activations
+//         (dssusan.co.kr page, the Figure 7 (a) passage);
+//   COL   128x1 groups (128 rows, one channel) stored transposed, the copy
+//         FP8 Wgrad consumes ("Is aI Hitting a Wall?", the Wgrad sentence);
+//   BLK   one 128x128 group: weights (same Figure 7 (a) passage), written
+//         as-is and/or transposed (the Dgrad operand).
+// Group scale: a = max(amax, 2^-100), s = a / 448, inv = 448 / a (IEEE
+// single divisions, no fast-math), code = E4M3_rn_satfinite(x * inv).
+// Row amax: warp shuffles over the 16 lanes sharing a row.  Column amax:
+// shuffle across the two 16-row halves, then shared memory across warps.
+// Codes leave as 8-byte row stores (a warp writes full 128-byte lines) and
+// 16-byte transposed stores (a warp writes full 32-byte sectors).
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8q {
+
+enum QuantMode : int {
+  kQRow = 1,    // 1x128 row groups   -> q_row[M][K], s_row[K/128][ld_srow]
+  kQCol = 2,    // 128x1 column groups -> q_colT[K][M], s_col[M/128][K]
+  kQBlk = 4,    // 128x128 block       -> q_blk[M][K], s_blk[M/128][K/128]
+  kQBlkT = 8,   // 128x128 block, transposed codes -> q_blkT[K][M], s_blkT[K/128][M/128]
+};
+
+struct QuantArgs {
+  const void* x;            // [rows_in][K] BF16 or FP32
+  int64_t M;                // rows of the (gathered) problem
+  int64_t K;                // columns, multiple of 128
+  const int32_t* src_rows;  // row gather (ROW mode only) or nullptr
+  uint8_t* q_row;
+  float* s_row;
+  int64_t ld_srow;          // row stride of s_row (= M)
+  uint8_t* q_colT;
+  float* s_col;
+  uint8_t* q_blk;
+  float* s_blk;
+  uint8_t* q_blkT;
+  float* s_blkT;
+};
+
+// 16 rows x 8 columns of the input held by one thread.
+template <bool kF32>
+struct Frag;
+
+template <>
+struct Frag<false> {  // BF16: 8 values per 16-byte word, kept packed
+  uint4 v[16];
+  __device__ __forceinline__ void load(const void* base, int64_t elem_off, int j) {
+    v[j] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem_off));
+  }
+  __device__ __forceinline__ void zero(int j) { v[j] = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float get(int j, int i) const {
+    const uint32_t w = (i < 2) ? v[j].x : (i < 4) ? v[j].y : (i < 6) ? v[j].z : v[j].w;
+    return (i & 1) ? bf16hi_to_f32(w) : bf16lo_to_f32(w);
+  }
+};
+
+template <>
+struct Frag<true> {  // FP32: 8 values in two 16-byte words
+  float4 v[16][2];
+  __device__ __forceinline__ void load(const void* base, int64_t elem_off, int j) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
+    v[j][0] = __ldg(p);
+    v[j][1] = __ldg(p + 1);
+  }
+  __device__ __forceinline__ void zero(int j) {
+    v[j][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    v[j][1] = v[j][0];
+  }
+  __device__ __forceinline__ float get(int j, int i) const {
+    const float4& h = v[j][i >> 2];
+    const int r = i & 3;
+    return r == 0 ? h.x : r == 1 ? h.y : r == 2 ? h.z : h.w;
+  }
+};
+
+// amax -> (s, inv).  IEEE round-to-nearest-even divisions (the build uses
+// -prec-div=true and no fast-math, so '/' is div.rn.f32).
+__device__ __forceinline__ void group_scale(float amax, float& s, float& inv) {
+  const float a = fmaxf(amax, 0x1p-100f);
+  s = __fdiv_rn(a, 448.0f);
+  inv = __fdiv_rn(448.0f, a);
+}
+
+template <bool kF32, int kMode>
+__global__ void __launch_bounds__(128) quant_tile_kernel(const QuantArgs args) {
+  constexpr bool kRow = (kMode & kQRow) != 0;
+  constexpr bool kCol = (kMode & kQCol) != 0;
+  constexpr bool kBlk = (kMode & (kQBlk | kQBlkT)) != 0;
+
+  __shared__ float s_red[4][128];  // per-warp column maxima
+  __shared__ float s_inv[128];     // per-column inverse scales
+  __shared__ float s_blkred[4];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 15;  // column chunk: tile columns c*8 .. c*8+7
+  const int g = lane >> 4;  // row half: tile rows warp*32 + g*16 + j
+  const int64_t K = args.K;
+  const int64_t kb = blockIdx.x;
+  const int64_t mb = blockIdx.y;
+  const int64_t k0 = kb * 128;
+  const int64_t m0 = mb * 128;
+  const int rbase = warp * 32 + g * 16;  // tile-local first row of this thread
+
+  // ---- load 16 rows x 8 columns ------------------------------------------
+  Frag<kF32> f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + rbase + j;
+    if (m < args.M) {
+      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
+      f.load(args.x, src * K + k0 + c * 8, j);
+    } else {
+      f.zero(j);
+    }
+  }
+
+  // ---- 1x128 row groups ----------------------------------------------------
+  if constexpr (kRow) {
+    float amax[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float a = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f.get(j, i)));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      amax[j] = a;
+    }
+    // lane c of each half computes the scale of row rbase + c ...
+    float mine = amax[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) mine = (c == j) ? amax[j] : mine;
+    float s, inv;
+    group_scale(mine, s, inv);
+    const int64_t my_m = m0 + rbase + c;
+    if (my_m < args.M) args.s_row[kb * args.ld_srow + my_m] = s;
+    // ... and hands its inverse to the other 15 lanes of the half
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float rinv = __shfl_sync(0xffffffffu, inv, (g << 4) | j);
+      const int64_t m = m0 + rbase + j;
+      const uint32_t w0 = cvt_e4m3x4(f.get(j, 0) * rinv, f.get(j, 1) * rinv, f.get(j, 2) * rinv, f.get(j, 3) * rinv);
+      const uint32_t w1 = cvt_e4m3x4(f.get(j, 4) * rinv, f.get(j, 5) * rinv, f.get(j, 6) * rinv, f.get(j, 7) * rinv);
+      if (m < args.M) {
+        *reinterpret_cast<uint2*>(args.q_row + m * K + k0 + c * 8) = make_uint2(w0, w1);
+      }
+    }
+  }
+
+  // ---- 128x1 column groups, stored transposed ------------------------------
+  if constexpr (kCol) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(f.get(j, i)));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+      if (g == 0) s_red[warp][c * 8 + i] = a;
+    }
+    __syncthreads();
+    {
+      const int t = threadIdx.x;  // column t of the tile
+      const float a = fmaxf(fmaxf(s_red[0][t], s_red[1][t]), fmaxf(s_red[2][t], s_red[3][t]));
+      float s, inv;
+      group_scale(a, s, inv);
+      args.s_col[mb * K + k0 + t] = s;
+      s_inv[t] = inv;
+    }
+    __syncthreads();
+    const int64_t ldT = args.M;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float cinv = s_inv[c * 8 + i];
+      uint32_t w[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        w[p] = cvt_e4m3x4(f.get(4 * p + 0, i) * cinv, f.get(4 * p + 1, i) * cinv, f.get(4 * p + 2, i) * cinv,
+                          f.get(4 * p + 3, i) * cinv);
+      }
+      *reinterpret_cast<uint4*>(args.q_colT + (k0 + c * 8 + i) * ldT + m0 + rbase) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+
+  // ---- 128x128 block -------------------------------------------------------
+  if constexpr (kBlk) {
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f.get(j, i)));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) s_blkred[warp] = a;
+    __syncthreads();
+    a = fmaxf(fmaxf(s_blkred[0], s_blkred[1]), fmaxf(s_blkred[2], s_blkred[3]));
+    float s, inv;
+    group_scale(a, s, inv);
+    const int64_t KB = K >> 7;
+    const int64_t MB = args.M >> 7;
+    if constexpr ((kMode & kQBlk) != 0) {
+      if (threadIdx.x == 0) args.s_blk[mb * KB + kb] = s;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int64_t m = m0 + rbase + j;
+        const uint32_t w0 = cvt_e4m3x4(f.get(j, 0) * inv, f.get(j, 1) * inv, f.get(j, 2) * inv, f.get(j, 3) * inv);
+        const uint32_t w1 = cvt_e4m3x4(f.get(j, 4) * inv, f.get(j, 5) * inv, f.get(j, 6) * inv, f.get(j, 7) * inv);
+        *reinterpret_cast<uint2*>(args.q_blk + m * K + k0 + c * 8) = make_uint2(w0, w1);
+      }
+    }
+    if constexpr ((kMode & kQBlkT) != 0) {
+      if (threadIdx.x == 0) args.s_blkT[kb * MB + mb] = s;
+      const int64_t ldT = args.M;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          w[p] = cvt_e4m3x4(f.get(4 * p + 0, i) * inv, f.get(4 * p + 1, i) * inv, f.get(4 * p + 2, i) * inv,
+                            f.get(4 * p + 3, i) * inv);
+        }
+        *reinterpret_cast<uint4*>(args.q_blkT + (k0 + c * 8 + i) * ldT + m0 + rbase) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+}  // namespace fp8q

@@ -1,0 +1,220 @@
+/*
+ * fp8q.h -- fine-grained FP8 (E4M3) quantization and block-scaled FP8 GEMM
+ * for NVIDIA B300 (sm_103a).  C ABI of libfp8q.so.
+ *
+ * The method (DeepSeek-V3 FP8 mixed-precision training, as retold by the
+ * scraped pages this library follows):
+ *  - activations are grouped and scaled per 1x128 tile (one token, 128
+ *    channels), weights per 128x128 block (128 input x 128 output channels)
+ *    -- dssusan.co.kr page, the Figure 7 (a) passage;
+ *  - E4M3 on all tensors, for Fprop, Dgrad and Wgrad alike
+ *    -- "Deepseek Ai News Expert Interview", the E4M3/E5M2 passage;
+ *  - all three Linear GEMMs run in FP8, take FP8 inputs and produce BF16 or
+ *    FP32 -- dssusan.co.kr page, the Figure 6 passage, and
+ *    "Deepseek Ai News Expert Interview", the GEMM input/output passage;
+ *  - tensor-core partial sums are promoted to FP32 on CUDA cores every 128
+ *    K-elements, where full-precision FP32 accumulation happens and the
+ *    dequantization scales are applied -- "Eliminate Deepseek Ai News For
+ *    Good", the MMA-precision passage; inprokorea.com page, the
+ *    accumulation-interval passage; "Is aI Hitting a Wall?", the
+ *    dequantization passage;
+ *  - activations are quantized before the MoE dispatch and the experts' FP8
+ *    up-projection takes every routed row (no token dropping)
+ *    -- "Eliminate Deepseek Ai News For Good", the dispatch passage;
+ *    inprokorea.com page, the no-token-dropping sentence.
+ *
+ * Numeric definitions (where the pages are silent, their plainest reading):
+ *  - E4M3 is E4M3FN: bias 7, no infinities, max finite 448.  Casts round to
+ *    nearest even and saturate to +-448; the sign of zero is kept.
+ *  - Each group: a = max(amax, 2^-100), s = a / 448 and inv = 448 / a (IEEE
+ *    single divisions), code = E4M3(x * inv) with x * inv rounded to FP32.
+ *    The stored scale s dequantizes: x ~ decode(code) * s.
+ *  - GEMM: C[m][n] = sum over K-blocks kb (ascending) of
+ *    sA(kb, m) * sB(kb, n) * P_kb[m][n], with P_kb the tensor-core sum over
+ *    the 128 k of block kb, promoted to FP32 registers each block.
+ *  Only finite inputs are defined; NaN/Inf propagate unspecified.
+ *
+ * Conventions common to every entry point:
+ *  - Every pointer argument is DEVICE memory (cudaMalloc'd or equivalent),
+ *    owned by the caller; the library never allocates or frees device
+ *    memory and keeps no pointer after the call returns.
+ *  - Every pointer must be 16-byte aligned.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream)
+ *    of the current device; nothing blocks except fp8q_get_device_status.
+ *  - Calls are stateless and may be made from several host threads.
+ *  - Argument errors are reported synchronously (nothing is launched):
+ *    FP8Q_ERR_NULL, FP8Q_ERR_SHAPE, FP8Q_ERR_ALIGN, FP8Q_ERR_DTYPE, and
+ *    FP8Q_ERR_DEVICE when the current device is not sm_103.  A failed launch
+ *    returns FP8Q_ERR_CUDA.  A kernel whose internal pipeline wait exceeds
+ *    its time limit (a bug, never expected) records FP8Q_ERR_TIMEOUT in a
+ *    device status word and exits early; fp8q_get_device_status reports it.
+ *  - Code layouts are row-major uint8 with the contraction dimension K
+ *    contiguous.  Scale arrays are FP32 and K-block-major: the scales one
+ *    K-block of a tile needs are contiguous.
+ *  - Sizes are int64_t element counts.  A zero-row problem is a no-op that
+ *    returns FP8Q_OK once the sizes and codes are valid; its pointers are
+ *    not inspected (empty buffers may be NULL).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* the CUDA runtime's cudaStream_t */
+struct CUstream_st;
+typedef struct CUstream_st *fp8q_stream_t;
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_NULL = 1,     /* a required pointer is NULL                      */
+    FP8Q_ERR_SHAPE = 2,    /* a size is negative or breaks a divisibility rule */
+    FP8Q_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned                */
+    FP8Q_ERR_DTYPE = 4,    /* unknown dtype / granularity code                */
+    FP8Q_ERR_DEVICE = 5,   /* current device is not sm_103 (B300)             */
+    FP8Q_ERR_CUDA = 6,     /* a CUDA call or launch failed                     */
+    FP8Q_ERR_TIMEOUT = 7   /* a kernel's pipeline wait timed out (device side) */
+} fp8q_status;
+
+typedef enum {
+    FP8Q_BF16 = 0,
+    FP8Q_FP32 = 1
+} fp8q_dtype;
+
+/*
+ * fp8q_quantize_act -- activation quantization, 1x128 tiles plus the 128x1
+ * transposed copy that Wgrad consumes.
+ *   x       [M][K] row-major, BF16 or FP32 (in_dtype).  K % 128 == 0.
+ *   q_row   [M][K] E4M3 codes of the 1x128 groups (one row, 128 channels).
+ *   s_row   [K/128][M] their scales.
+ *   q_colT  [K][M] E4M3 codes of the 128x1 groups (128 consecutive rows of
+ *           one column of the ORIGINAL x), stored transposed: row k holds
+ *           column k of x, token index contiguous.  Requires M % 128 == 0.
+ *   s_col   [M/128][K] their scales.
+ * Either output pair may be (NULL, NULL) to skip it, not both; a pair must
+ * be both set or both NULL.  Codes and scales are bit-exact functions of x.
+ * Groups: dssusan.co.kr page, the Figure 7 (a) passage; the transposed copy
+ * serves FP8 Wgrad with activations cached in FP8 ("Is aI Hitting a Wall?",
+ * the Wgrad/caching sentence).
+ */
+FP8Q_API int fp8q_quantize_act(const void *x, int in_dtype, int64_t M, int64_t K,
+                      uint8_t *q_row, float *s_row, uint8_t *q_colT, float *s_col,
+                      fp8q_stream_t stream);
+
+/*
+ * fp8q_quantize_act_gather -- 1x128 quantization fused with the MoE dispatch
+ * permutation: output row r is the quantization of input row src_rows[r].
+ *   x         [M][K] row-major, BF16 or FP32.  K % 128 == 0.
+ *   src_rows  [R] int32 device array, each in [0, M).  Out-of-range indices
+ *             are not checked on the device (the caller validates).
+ *   q_row     [R][K] codes;  s_row [K/128][R] scales.
+ * Equal, bit for bit, to quantize-then-gather, because 1x128 groups are
+ * row-local.  Quantize before dispatch: "Eliminate Deepseek Ai News For
+ * Good", the dispatch passage.
+ */
+FP8Q_API int fp8q_quantize_act_gather(const void *x, int in_dtype, int64_t M, int64_t K,
+                             const int32_t *src_rows, int64_t R,
+                             uint8_t *q_row, float *s_row, fp8q_stream_t stream);
+
+/*
+ * fp8q_quantize_weight -- 128x128 block quantization of a weight in PyTorch
+ * Linear layout.
+ *   w  [N][K] row-major (N output channels, K input channels), BF16 or FP32.
+ *      N % 128 == 0, K % 128 == 0.
+ *   q  [N][K] E4M3 codes;  s [N/128][K/128] block scales.
+ * Blocks: dssusan.co.kr page, the Figure 7 (a) passage.
+ */
+FP8Q_API int fp8q_quantize_weight(const void *w, int in_dtype, int64_t N, int64_t K,
+                         uint8_t *q, float *s, fp8q_stream_t stream);
+
+/*
+ * fp8q_quantize_weight_ex -- as fp8q_quantize_weight, and optionally also
+ * writes the transposed codes and scales that Dgrad (dX = dY . W) uses as
+ * its B operand:
+ *   q_t [K][N] codes of w^T (same block scales: a 128x128 block's scale does
+ *        not change under transposition);  s_t [K/128][N/128].
+ * Any of the pairs (q, s), (q_t, s_t) may be (NULL, NULL), not both.
+ * Dgrad in FP8: dssusan.co.kr page, the Figure 6 passage.
+ */
+FP8Q_API int fp8q_quantize_weight_ex(const void *w, int in_dtype, int64_t N, int64_t K,
+                            uint8_t *q, float *s, uint8_t *q_t, float *s_t,
+                            fp8q_stream_t stream);
+
+/*
+ * fp8q_gemm -- block-scaled FP8 GEMM with FP32 promotion every 128 K.
+ *   Aq  [M][K] E4M3 codes, K contiguous (1x128-quantized rows).
+ *   sA  [K/128][M] scales of A.
+ *   Bq  [N][K] E4M3 codes, K contiguous (a weight in Linear layout).
+ *   sB  [N/128][K/128] 128x128 block scales of B.
+ *   C   [M][N] row-major output, BF16 (rounded to nearest even) or FP32
+ *       (out_dtype).
+ *   C[m][n] = sum_kb sA[kb][m] * sB[n/128][kb] * P_kb[m][n].
+ * M >= 0 (any), N % 128 == 0, K % 128 == 0, K > 0.
+ * Accuracy: |C - C*| <= 2e-3 * sum_k |a_dq * b_dq| per element against the
+ * exact result C* (plus one BF16 rounding for BF16 output).
+ */
+FP8Q_API int fp8q_gemm(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
+              void *C, int64_t M, int64_t N, int64_t K, int out_dtype,
+              fp8q_stream_t stream);
+
+/*
+ * fp8q_gemm_ex -- fp8q_gemm with a choice of B-scale granularity along N:
+ *   sb_gran_n == 128: sB is [N/128][K/128] (as fp8q_gemm);
+ *   sb_gran_n == 1:   sB is [K/128][N], one scale per column n and K-block,
+ *                     the layout of fp8q_quantize_act's s_col.  This is
+ *                     Wgrad: dW = dY^T . X with both operands quantized in
+ *                     128x1 groups along the token (K) dimension, i.e.
+ *                     Aq = q_colT(dY), sA = s_col(dY), Bq = q_colT(X),
+ *                     sB = s_col(X).
+ */
+FP8Q_API int fp8q_gemm_ex(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
+                 void *C, int64_t M, int64_t N, int64_t K, int out_dtype,
+                 int sb_gran_n, fp8q_stream_t stream);
+
+/*
+ * fp8q_grouped_gemm -- MoE grouped block-scaled FP8 GEMM over E experts with
+ * ragged rows (no token dropping).
+ *   Aq           [total_rows][K] codes of the dispatched (expert-grouped) rows.
+ *   sA           [K/128][total_rows] their scales.
+ *   Bq           [E][N][K] expert weights' codes;  sB [E][N/128][K/128].
+ *   C            [total_rows][N] output (BF16 or FP32).
+ *   row_offsets  [E+1] int32 DEVICE array: rows [off[e], off[e+1]) belong to
+ *                expert e; nondecreasing, off[0] == 0, off[E] == total_rows.
+ *                Read on the device (no host synchronization); the library
+ *                trusts it (it cannot check device contents without a sync).
+ * Empty experts are allowed and write nothing.  Rows of expert e are
+ * C[r] = (Aq[r], sA[:, r]) x (Bq[e], sB[e]) as in fp8q_gemm.
+ * N % 128 == 0, K % 128 == 0, E >= 1, total_rows >= 0.
+ */
+FP8Q_API int fp8q_grouped_gemm(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
+                      void *C, const int32_t *row_offsets, int32_t E, int64_t total_rows,
+                      int64_t N, int64_t K, int out_dtype, fp8q_stream_t stream);
+
+/*
+ * fp8q_get_device_status -- synchronizes `stream`, then returns and clears
+ * the current device's status word: FP8Q_OK, or FP8Q_ERR_TIMEOUT if a
+ * kernel's bounded pipeline wait expired since the last call, or
+ * FP8Q_ERR_CUDA if the synchronization itself failed.
+ */
+FP8Q_API int fp8q_get_device_status(fp8q_stream_t stream);
+
+/* fp8q_status_string -- static human-readable text for a status code. */
+FP8Q_API const char *fp8q_status_string(int status);
+
+/* fp8q_version -- library version as 10000*major + 100*minor + patch. */
+FP8Q_API int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

@@ -113,6 +113,7 @@ __attribute__((constructor)) static void build_decode_table(void)
 
 void oracle_e4m3_encode_array(const float *v, int64_t n, uint8_t *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_e4m3_encode(v[i]);
 }
