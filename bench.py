@@ -2,6 +2,7 @@
 """Benchmark of the fine-grained FP8 hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fp8q|reference]
+                    [--case all|fprop|act|wgrad|moe]
 
 One step = one FP8 Fprop pass of the dense FFN up-projection
 (tokens 4096, hidden 7168 -> 18432): quantize X (BF16 4096x7168, 1x128
@@ -14,12 +15,16 @@ exceed the 126 MB L2, so no flush is needed).  The JSON line also carries:
   e2e           the same metric through the C ABI with host buffers: pinned
                 H2D copies of X and W, the three kernels, D2H of Y per step
   breakdown     activation quantization 16384x7168 (GB/s vs HBM), Wgrad
-                2048x7168x8192 and the 256-expert MoE grouped GEMM (TFLOP/s)
+                2048x7168x8192 and the 256-expert MoE grouped GEMM (TFLOP/s),
+                each with its own roofline
   cpu_baseline  the CPU oracle on a bounded sample of the same step
-  clocks        NVML samples of SM clock and throttle reasons while timing
-`--impl reference` times the CPU oracle (the reference of this build) on a
-bounded sample of each step instead.  Under torchrun every rank runs an
-independent replica (no collective on the data path); value sums ranks.
+  clocks        nvidia-smi samples of SM clock and throttle reasons taken
+                while the timed region runs
+`--case X` (X other than all) times one workload alone and prints its
+numbers; the profiling commands use it.  `--impl reference` times the CPU
+oracle (the reference of this build) on a bounded sample of each step
+instead.  Under torchrun every rank runs an independent replica (no
+collective on the data path); value sums ranks.
 """
 import argparse
 import hashlib
@@ -40,17 +45,24 @@ WGRAD = dict(T=8192, Dout=2048, Din=7168)
 MOE = dict(T=8192, H=7168, E=256, N=2048, topk=8)
 METRIC = "FP8 blockscaled GEMM TFLOP/s (% B300 dense FP8 peak); quantize GB/s (% HBM)"
 FP8_PER_BF16 = 2.0  # nominal dense ratio: 4.5 PFLOP/s FP8 / 2.25 PFLOP/s BF16
+FPROP_WORKLOAD = ("fprop 4096x18432x7168: quantize X 1x128 + quantize W 128x128 + block-scaled FP8 GEMM, "
+                  "BF16 out")
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
+    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe"],
+                   help="all: the Fprop step plus the breakdown; else time one workload alone")
     p.add_argument("--no-breakdown", action="store_true", help="time the Fprop step only")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--ref-budget", type=float, default=90.0,
+                   help="seconds of oracle work for the whole --impl reference run")
     return p.parse_args()
 
 
@@ -66,6 +78,8 @@ def peaks():
 
 
 def kernel_sha():
+    """Hash of the CUDA sources: a recorded ncu traffic figure is used only
+    while the kernels are the ones it was taken of."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fine_grained_fp8_quantize_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
@@ -75,8 +89,9 @@ def kernel_sha():
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken of
-    the current kernel sources (else None)."""
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from a committed ncu capture, if it was taken of the current kernel
+    sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -92,70 +107,161 @@ def recorded_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """Polls NVML (SM clock, max clock, throttle reasons) in a thread."""
+    """Samples SM clock, max clock, power and throttle reasons with
+    ``nvidia-smi -lms`` while the timed region runs; only samples taken
+    between mark_start() and mark_stop() (host wall clock) are kept."""
 
-    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
-               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle"}
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index):
-        self.samples = []
-        self.reasons = 0
-        self.ok = False
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.max_mhz = None
-        self._stop = threading.Event()
-
-    def _run(self):
-        nv = self.nv
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                get = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                    nv.nvmlDeviceGetCurrentClocksThrottleReasons
-                self.reasons |= get(self.h)
-            except Exception:
-                pass
-            time.sleep(0.002)
+    def __init__(self, index, period_ms=50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.lines = []
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.6)  # let nvidia-smi start sampling before the timed region
+        except OSError:
+            self.proc = None
         return self
 
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.reader.join(timeout=5)
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": len(self.samples)}
-        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
-        return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples)}
+        mhz, maxes, watts, reasons = [], [], [], set()
+        for t, line in self.lines:
+            if self.t0 is None or not (self.t0 <= t <= (self.t1 or t)):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+                watts.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(self.REASONS, parts[4:]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi samples inside the timed region"}
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": float(max(maxes)), "reasons": sorted(reasons),
+                "samples": len(mhz), "power_w_median": float(np.median(watts))}
 
 
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def gpu_arm(args, rank, world, dist):
-    import torch
+def fp8_peak(pk):
+    return pk["bf16"] * FP8_PER_BF16
 
-    import fine_grained_fp8_quantize_b300 as f
-    import synth
 
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+def tensor_roofline(kernel, flops, ms, pk, workload):
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = fp8_peak(pk)
+    return {"kernel": kernel, "bound": "tensor", "achieved": round(tf, 1), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+            "peak_note": "%s BF16 matmul burst %.1f TFLOP/s x 2 (nominal FP8:BF16 dense ratio), 'of %s'; "
+                         "frac vs sustained x 2 = %.4f; vs nominal 4.5 PFLOP/s = %.4f"
+                         % (pk["src"], pk["bf16"], pk["src"], tf / (pk["bf16_sus"] * FP8_PER_BF16), tf / 4500.0),
+            "ms_per_launch": round(ms, 5), "flops_per_launch": flops,
+            "traffic": recorded_traffic(kernel.split("<")[0], workload)}
+
+
+def hbm_roofline(kernel, nbytes, ms, pk, workload):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(gbs / pk["hbm"], 4),
+            "peak_note": "%s STREAM-style copy; vs 8 TB/s nominal = %.4f" % (pk["src"], gbs / 8000.0),
+            "ms_per_launch": round(ms, 5), "bytes_per_launch": nbytes,
+            "traffic": recorded_traffic(kernel.split("<")[0], workload)}
+
+
+class Timed:
+    """Per-launch CUDA-event timing of one kernel inside a step, on the
+    stream the kernel is launched on."""
+
+    def __init__(self, torch, n):
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+        self.i = 0
+
+    def __call__(self, stream, fn):
+        a, b = self.ev[self.i]
+        a.record(stream)
+        fn()
+        b.record(stream)
+        self.i += 1
+
+    def mean_ms(self):
+        return float(np.mean([a.elapsed_time(b) for a, b in self.ev[:self.i]]))
+
+
+def check_status(f, when):
+    st = f.fp8q_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status %s: %s" % (when, f.fp8q_status_string(st)))
+
+
+def run_timed(torch, stream, step, steps, warmup, dist=None):
+    """Warm-up, then exactly `steps` steps bracketed by barrier + synchronize,
+    with clocks sampled during the timed region.  -> (ms total, clocks)."""
+    for _ in range(warmup):
+        step(False)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        sampler.mark_start()
+        t0.record(stream)
+        for _ in range(steps):
+            step(True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        sampler.mark_stop()
+        if dist:
+            dist.barrier()
+    return t0.elapsed_time(t1), sampler.summary()
+
+
+def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
     stream = torch.cuda.current_stream()
-    pk = peaks()
     M, N, K = FPROP["M"], FPROP["N"], FPROP["K"]
     flops = 2.0 * M * N * K
 
@@ -165,83 +271,37 @@ def gpu_arm(args, rank, world, dist):
     qw = torch.empty(N, K, dtype=torch.uint8, device="cuda")
     sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device="cuda")
     Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    tg = Timed(torch, args.steps)
 
-    def step(ev=None):
+    def step(timed):
         f.fp8q_quantize_act(X, qx, sx)
         f.fp8q_quantize_weight(W, qw, sw)
-        if ev is not None:
-            ev[0].record(stream)
-        f.fp8q_gemm(qx, sx, qw, sw, Y)
-        if ev is not None:
-            ev[1].record(stream)
+        if timed:
+            tg(stream, lambda: f.fp8q_gemm(qx, sx, qw, sw, Y))
+        else:
+            f.fp8q_gemm(qx, sx, qw, sw, Y)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st = f.fp8q_get_device_status()
-    if st != 0:
-        raise RuntimeError("device status after warm-up: %s" % f.fp8q_status_string(st))
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device())
-    with sampler:
-        t0.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = t0.elapsed_time(t1)
-    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    ms, clocks = run_timed(torch, stream, step, args.steps, args.warmup, dist)
+    check_status(f, "after the fprop timing")
     if dist:
         tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    st = f.fp8q_get_device_status()
-    if st != 0:
-        raise RuntimeError("device status after timing: %s" % f.fp8q_status_string(st))
-
-    ms_step = ms / args.steps
     value = world * flops * args.steps / (ms * 1e-3) / 1e12
-    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    peak_fp8 = pk["bf16"] * FP8_PER_BF16
-    roofline = {
-        "kernel": "gemm_kernel<bf16 out, 128x128 B scales>",
-        "bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
-        "frac": round(gemm_tflops / peak_fp8, 4),
-        "peak_note": "%s BF16 matmul burst %.1f TFLOP/s x 2 (nominal FP8:BF16); frac vs sustained x2 = %.4f"
-                     % (pk["src"], pk["bf16"], gemm_tflops / (pk["bf16_sus"] * FP8_PER_BF16)),
-        "gemm_ms": round(gemm_ms, 4), "flops_per_launch": flops,
-        "traffic": recorded_traffic("gemm_kernel", "fprop_4096x18432x7168"),
-    }
-
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
         "data": "synthetic (seeded SplitMix64 + Box-Muller; X N(0,1) with 0.1% x1e3, W N(0,0.02^2))",
-        "config": {"workload": "fprop 4096x18432x7168: quantize X 1x128 + quantize W 128x128 + block-scaled "
-                               "FP8 GEMM, BF16 out", "M": M, "N": N, "K": K, "global_batch": M * world,
+        "config": {"workload": FPROP_WORKLOAD, "M": M, "N": N, "K": K, "global_batch": M * world,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (323 MB BF16 per step), no flush"},
-        "roofline": roofline,
+        "roofline": tensor_roofline("gemm_kernel<bf16 out, 128x128 B scales>", flops, tg.mean_ms(), pk,
+                                    "fprop_4096x18432x7168"),
         "gpu_launches": 3 * args.steps,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
     }
-
-    if rank == 0 and not args.no_e2e:
-        out["e2e"] = e2e_fprop(args, f, torch, X, W)
-    if rank == 0 and not args.no_breakdown:
-        out["breakdown"] = breakdown(args, f, torch, synth, pk)
-    if rank == 0 and not args.no_cpu:
-        out["cpu_baseline"] = cpu_baseline_fprop(X, W, budget_s=15.0)
-    return out
+    return out, X, W
 
 
 def e2e_fprop(args, f, torch, X, W):
@@ -286,7 +346,9 @@ def e2e_fprop(args, f, torch, X, W):
             "d2h_bytes_per_step": M * N * 2}
 
 
-def _time(fn, iters, torch, warm=3):
+def _time(torch, fn, iters, warm=3):
+    """Mean ms per call of fn over `iters` back-to-back calls (events on the
+    current stream, which is where the library launches)."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
@@ -299,27 +361,23 @@ def _time(fn, iters, torch, warm=3):
     return a.elapsed_time(b) / iters
 
 
-def breakdown(args, f, torch, synth, pk):
-    res = {}
-    iters = max(5, min(args.steps, 50))
-    # -- activation quantization, 16384 x 7168, 1x128 rows + 128x1 transposed copy
+def case_act(args, f, torch, synth, pk, iters):
+    """Activation quantization 16384x7168: 1x128 rows + 128x1 transposed copy."""
     T, H = ACT["T"], ACT["H"]
     X = synth.act_quant_inputs(device="cuda")
     q_row = torch.empty(T, H, dtype=torch.uint8, device="cuda")
     s_row = torch.empty(H // 128, T, dtype=torch.float32, device="cuda")
     q_colT = torch.empty(H, T, dtype=torch.uint8, device="cuda")
     s_col = torch.empty(T // 128, H, dtype=torch.float32, device="cuda")
-    ms = _time(lambda: f.fp8q_quantize_act(X, q_row, s_row, q_colT, s_col), iters, torch)
+    ms = _time(torch, lambda: f.fp8q_quantize_act(X, q_row, s_row, q_colT, s_col), iters)
+    check_status(f, "after the activation quantization")
     nbytes = T * H * 2 + 2 * T * H + 2 * (T * H // 128) * 4
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    res["act_quant_16384x7168"] = {
-        "ms": round(ms, 4), "GB/s": round(gbs, 1), "bytes": nbytes,
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm"], 4), "frac_of_8TBs_nominal": round(gbs / 8000.0, 4),
-                     "traffic": recorded_traffic("quant_tile_kernel", "act_16384x7168")}}
-    del X, q_row, s_row, q_colT, s_col
+    return {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes,
+            "roofline": hbm_roofline("quant_tile_kernel<bf16, row|col>", nbytes, ms, pk, "act_16384x7168")}
 
-    # -- Wgrad: dW = dY^T X, 128x1 groups along 8192 tokens, FP32 out
+
+def case_wgrad(args, f, torch, synth, pk, iters):
+    """Wgrad dW = dY^T X: 128x1 groups along 8192 tokens, FP32 out."""
     dY, Xw = synth.wgrad_inputs(device="cuda")
     Tt, Do, Di = WGRAD["T"], WGRAD["Dout"], WGRAD["Din"]
     qdy = torch.empty(Do, Tt, dtype=torch.uint8, device="cuda")
@@ -329,23 +387,27 @@ def breakdown(args, f, torch, synth, pk):
     dW = torch.empty(Do, Di, dtype=torch.float32, device="cuda")
     f.fp8q_quantize_act(dY, None, None, qdy, sdy)
     f.fp8q_quantize_act(Xw, None, None, qx, sx)
-    ms_g = _time(lambda: f.fp8q_gemm_ex(qdy, sdy, qx, sx, dW, 1), iters, torch)
-    ms_all = _time(lambda: (f.fp8q_quantize_act(dY, None, None, qdy, sdy), f.fp8q_quantize_act(Xw, None, None, qx, sx),
-                            f.fp8q_gemm_ex(qdy, sdy, qx, sx, dW, 1)), iters, torch)
+    ms_g = _time(torch, lambda: f.fp8q_gemm_ex(qdy, sdy, qx, sx, dW, 1), iters)
+    ms_all = _time(torch, lambda: (f.fp8q_quantize_act(dY, None, None, qdy, sdy),
+                                   f.fp8q_quantize_act(Xw, None, None, qx, sx),
+                                   f.fp8q_gemm_ex(qdy, sdy, qx, sx, dW, 1)), iters)
+    check_status(f, "after wgrad")
     fl = 2.0 * Do * Di * Tt
-    res["wgrad_2048x7168x8192"] = {
-        "gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1),
-        "step_ms": round(ms_all, 4), "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
-        "frac_of_fp8_peak": round(fl / ms_g / 1e9 / (pk["bf16"] * FP8_PER_BF16), 4)}
-    del dY, Xw, qdy, sdy, qx, sx, dW
+    return {"gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1),
+            "step_ms": round(ms_all, 4), "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
+            "roofline": tensor_roofline("gemm_kernel<f32 out, per-column B scales>", fl, ms_g, pk,
+                                        "wgrad_2048x7168x8192")}
 
-    # -- MoE grouped GEMM: 8192 tokens, 256 experts (top-8), 7168 -> 2048, BF16 out
+
+def case_moe(args, f, torch, synth, pk, iters):
+    """MoE grouped GEMM: 8192 tokens, 256 experts (top-8), 7168 -> 2048, BF16 out."""
     off, src = synth.moe_routing()
     counts = off[1:] - off[:-1]
     active = [int(e) for e in np.flatnonzero(counts)]
     E, Nn, Kk = MOE["E"], MOE["N"], MOE["H"]
     Xm, Wm = synth.moe_inputs(device="cuda", experts=active)
     qw, sw = f.quantize_weight(Wm.view(E * Nn, Kk))
+    del Wm
     qw = qw.view(E, Nn, Kk)
     sw = sw.view(E, Nn // 128, Kk // 128)
     src_d = torch.from_numpy(src.astype(np.int32)).cuda()
@@ -355,44 +417,86 @@ def breakdown(args, f, torch, synth, pk):
     sa = torch.empty(Kk // 128, R, dtype=torch.float32, device="cuda")
     Cm = torch.empty(R, Nn, dtype=torch.bfloat16, device="cuda")
     f.fp8q_quantize_act_gather(Xm, src_d, qa, sa)
-    ms_g = _time(lambda: f.fp8q_grouped_gemm(qa, sa, qw, sw, Cm, off_d), iters, torch)
-    ms_all = _time(lambda: (f.fp8q_quantize_act_gather(Xm, src_d, qa, sa),
-                            f.fp8q_grouped_gemm(qa, sa, qw, sw, Cm, off_d)), iters, torch)
+    ms_g = _time(torch, lambda: f.fp8q_grouped_gemm(qa, sa, qw, sw, Cm, off_d), iters)
+    ms_all = _time(torch, lambda: (f.fp8q_quantize_act_gather(Xm, src_d, qa, sa),
+                                   f.fp8q_grouped_gemm(qa, sa, qw, sw, Cm, off_d)), iters)
+    check_status(f, "after moe")
     fl = 2.0 * R * Nn * Kk
-    wbytes = len(active) * Nn * Kk
+    wbytes = len(active) * (Nn * Kk + (Nn // 128) * (Kk // 128) * 4)
     gbytes = R * Kk + R * (Kk // 128) * 4 + wbytes + R * Nn * 2
-    t_comp = fl / (pk["bf16"] * FP8_PER_BF16 * 1e12)
+    t_comp = fl / (fp8_peak(pk) * 1e12)
     t_mem = gbytes / (pk["hbm"] * 1e9)
-    res["moe_grouped_256x(7168->2048)"] = {
-        "active_experts": len(active), "rows": R, "gemm_ms": round(ms_g, 4),
-        "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
-        "bound": "tensor" if t_comp > t_mem else "hbm",
-        "roofline_frac": round(max(t_comp, t_mem) / (ms_g * 1e-3), 4),
-        "min_bytes": gbytes}
-    return res
+    return {"active_experts": len(active), "rows": R, "max_rows_per_expert": int(counts.max()),
+            "gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
+            "bound": "tensor" if t_comp > t_mem else "hbm",
+            "roofline_frac": round(max(t_comp, t_mem) / (ms_g * 1e-3), 4), "min_bytes": gbytes,
+            "roofline": tensor_roofline("gemm_kernel<bf16 out, grouped>", fl, ms_g, pk, "moe_256x2048x7168")}
 
 
-def cpu_baseline_fprop(X, W, budget_s=15.0):
-    """The CPU oracle as it stands on a bounded sample of the Fprop step:
-    quantize R rows of X and all of W, then compute R full output rows."""
+CASES = {"act_quant_16384x7168": case_act, "wgrad_2048x7168x8192": case_wgrad,
+         "moe_grouped_256x(7168->2048)": case_moe}
+CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)"}
+
+
+def oracle_fprop_sample(xb, wb, R, C):
+    """The CPU oracle as it stands on a slice of the Fprop step: quantize R
+    rows of X (1x128), quantize the first C rows of W (C/128 row-blocks of
+    128x128 blocks), compute the R x C outputs.  -> (seconds, FLOPs)."""
+    import oracle
+    K = FPROP["K"]
+    t = time.perf_counter()
+    qx, sx = oracle.quantize_act_rows(xb[:R])
+    qw, sw = oracle.quantize_weight(wb[:C])
+    mi = np.repeat(np.arange(R), C)
+    ni = np.tile(np.arange(C), R)
+    oracle.gemm_points(qx, sx, qw, sw, mi, ni)
+    return time.perf_counter() - t, 2.0 * R * C * K
+
+
+def oracle_sample_size(xb, wb, seconds):
+    """(R, C) whose oracle_fprop_sample takes about `seconds`, calibrated on
+    a small slice; R rows of X and C (a multiple of 128) output columns."""
+    M, N = FPROP["M"], FPROP["N"]
+    dt, _ = oracle_fprop_sample(xb, wb, 4, 512)
+    scale = max(seconds / max(dt, 1e-4), 1e-3)
+    C = int(min(N, max(128, 512 * min(scale, N / 512.0)) // 128 * 128))
+    R = int(min(M, max(1, round(4 * scale * 512.0 / C))))
+    return R, C
+
+
+def cpu_baseline_fprop(X, W, budget_s):
     import oracle
     import synth
-    M, N, K = FPROP["M"], FPROP["N"], FPROP["K"]
-    xb = synth.bf16_bits(X)
-    wb = synth.bf16_bits(W)
-    R = 8
-    t = time.perf_counter()
-    rows = np.arange(0, M, M // R)[:R]
-    qx, sx = oracle.quantize_act_rows(xb[rows])
-    qw, sw = oracle.quantize_weight(wb)
-    mi = np.repeat(np.arange(R), N)
-    ni = np.tile(np.arange(N), R)
-    oracle.gemm_points(qx, sx, qw, sw, mi, ni)
-    dt = time.perf_counter() - t
-    fl = 2.0 * R * N * K
+    xb, wb = synth.bf16_bits(X), synth.bf16_bits(W)
+    R, C = oracle_sample_size(xb, wb, budget_s)
+    dt, fl = oracle_fprop_sample(xb, wb, R, C)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d of 4096 rows of the fprop step (quantize those rows, quantize all of W, %d full output "
-                      "rows); %.1f s" % (R, R, dt)}
+            "sample": "%d of 4096 rows x %d of 18432 columns of the fprop step: quantize those rows of X and "
+                      "those %d rows of W, compute the %dx%d outputs; %.1f s" % (R, C, C, R, C, dt)}
+
+
+def gpu_arm(args, rank, world, dist):
+    import torch
+
+    import fine_grained_fp8_quantize_b300 as f
+    import synth
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    pk = peaks()
+    iters = max(5, min(args.steps, 50))
+    if args.case not in ("all", "fprop"):
+        key = CASE_KEYS[args.case]
+        return {"case": key, **CASES[key](args, f, torch, synth, pk, iters)}
+    out, X, W = gpu_fprop(args, rank, world, dist, f, torch, synth, pk)
+    if args.case == "fprop":
+        return out
+    if rank == 0 and not args.no_e2e:
+        out["e2e"] = e2e_fprop(args, f, torch, X, W)
+    if rank == 0 and not args.no_breakdown:
+        out["breakdown"] = {k: fn(args, f, torch, synth, pk, iters) for k, fn in CASES.items()}
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_fprop(X, W, args.cpu_budget)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -402,34 +506,26 @@ def cpu_baseline_fprop(X, W, budget_s=15.0):
 def reference_arm(args):
     import oracle
     import synth
-    import torch
     M, N, K = FPROP["M"], FPROP["N"], FPROP["K"]
-    R = 4
-    X = synth.matrix(2, 1, R, K, 1.0, entry_frac=1e-3, entry_scale=1e3)   # rows of the fprop X
-    W = synth.matrix(2, 2, N, K, 0.02)
+    X, W = synth.fprop_inputs(device="cpu", seed=2, M=64, N=N, K=K)
     xb, wb = synth.bf16_bits(X), synth.bf16_bits(W)
-    mi = np.repeat(np.arange(R), N)
-    ni = np.tile(np.arange(N), R)
-
-    def step():
-        qx, sx = oracle.quantize_act_rows(xb)
-        qw, sw = oracle.quantize_weight(wb)
-        oracle.gemm_points(qx, sx, qw, sw, mi, ni)
-
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    R, C = oracle_sample_size(xb, wb, per_step)
     for _ in range(args.warmup):
-        step()
-    t = time.perf_counter()
+        oracle_fprop_sample(xb, wb, R, C)
+    tot, fl = 0.0, 0.0
     for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t) / args.steps
-    fl = 2.0 * R * N * K
-    v = fl / dt / 1e12
-    sample = "%d of 4096 rows of the fprop step per step (quantize them and all of W, %d full output rows)" % (R, R)
+        dt, f_ = oracle_fprop_sample(xb, wb, R, C)
+        tot += dt
+        fl += f_
+    v = fl / tot / 1e12
+    sample = ("per step: %d of 4096 rows x %d of 18432 columns of the fprop step (quantize those rows of X and "
+              "those rows of W, compute the %dx%d outputs)" % (R, C, R, C))
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 exact / f32 promotion order (CPU)",
-            "data": "synthetic", "config": {"workload": "fprop 4096x18432x7168 (bounded row sample)",
-                                            "M": M, "N": N, "K": K},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 exact / f32 promotion order (CPU)", "data": "synthetic",
+            "config": {"workload": FPROP_WORKLOAD + " (bounded sample per step)", "M": M, "N": N, "K": K},
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
