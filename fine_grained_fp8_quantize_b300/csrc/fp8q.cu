@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "fp8q.h"
@@ -91,6 +92,22 @@ bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
+// 2-D output tensor C [rows][cols] (BF16 or FP32, cols contiguous) for TMA
+// stores of 32-row x 32-byte boxes, no swizzle.
+bool make_tmap_out(CUtensorMap* tm, void* base, bool f32, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t esize = f32 ? 4u : 2u;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esize};
+  cuuint32_t box[2] = {32u / esize, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int launch_status() { return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA; }
 
 template <bool kF32, int kMode>
@@ -101,19 +118,51 @@ int launch_quant(const QuantArgs& a, int64_t grid_x, int64_t grid_y, cudaStream_
   return launch_status();
 }
 
+// BF16 input: the persistent double-buffered kernel, as many CTAs as fit on
+// the device at once (occupancy probed once per device).
+template <int kMode>
+int launch_quant_pipe(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  DeviceInfo di;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  auto kern = quant_pipe_kernel<kMode>;
+  constexpr int kSmem = 2 * kPipeTileBytes;
+  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, kSmem) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  kern<<<grid, 128, kSmem, stream>>>(a, tiles);
+  return launch_status();
+}
+
+// FP32 input, and BF16 rows + transposed columns in one pass (whose register
+// need allows 2 pipelined CTAs per SM, fewer than the 3 direct-load CTAs that
+// measure faster): one CTA per tile.  Other BF16 modes: the pipelined kernel.
 template <int kMode>
 int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cudaStream_t s) {
-  return in_dtype == FP8Q_FP32 ? launch_quant<true, kMode>(a, gx, gy, s) : launch_quant<false, kMode>(a, gx, gy, s);
+  if (in_dtype == FP8Q_FP32) return launch_quant<true, kMode>(a, gx, gy, s);
+  if (kMode == (kQRow | kQCol)) return launch_quant<false, kMode>(a, gx, gy, s);
+  return launch_quant_pipe<kMode>(a, gx * gy, s);
 }
 
 template <bool kOutF32, int kSbGran, bool kGrouped>
-int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
+                  cudaStream_t s) {
   auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped>;
   const uint32_t smem = kGrouped ? kSmemGrouped : kSmemDense;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return FP8Q_ERR_CUDA;
-  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, a);
+  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, tc, a);
   return launch_status();
 }
 
@@ -141,6 +190,9 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   if (!make_tmap_u8(&ta, Aq, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM)) return FP8Q_ERR_CUDA;
   const uint64_t brows = grouped ? static_cast<uint64_t>(E) * N : static_cast<uint64_t>(N);
   if (!make_tmap_u8(&tb, Bq, static_cast<uint64_t>(K), brows, kBN)) return FP8Q_ERR_CUDA;
+  CUtensorMap tc;
+  if (!make_tmap_out(&tc, C, out_dtype == FP8Q_FP32, static_cast<uint64_t>(N), static_cast<uint64_t>(M)))
+    return FP8Q_ERR_CUDA;
 
   GemmArgs a;
   a.sA = sA;
@@ -165,15 +217,15 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   const int grid = static_cast<int>(tiles_upper < di.sms ? tiles_upper : di.sms);
   const bool f32 = out_dtype == FP8Q_FP32;
   if (grouped) {
-    return f32 ? launch_gemm_t<true, 128, true>(ta, tb, a, grid, stream)
-               : launch_gemm_t<false, 128, true>(ta, tb, a, grid, stream);
+    return f32 ? launch_gemm_t<true, 128, true>(ta, tb, tc, a, grid, stream)
+               : launch_gemm_t<false, 128, true>(ta, tb, tc, a, grid, stream);
   }
   if (sb_gran == 1) {
-    return f32 ? launch_gemm_t<true, 1, false>(ta, tb, a, grid, stream)
-               : launch_gemm_t<false, 1, false>(ta, tb, a, grid, stream);
+    return f32 ? launch_gemm_t<true, 1, false>(ta, tb, tc, a, grid, stream)
+               : launch_gemm_t<false, 1, false>(ta, tb, tc, a, grid, stream);
   }
-  return f32 ? launch_gemm_t<true, 128, false>(ta, tb, a, grid, stream)
-             : launch_gemm_t<false, 128, false>(ta, tb, a, grid, stream);
+  return f32 ? launch_gemm_t<true, 128, false>(ta, tb, tc, a, grid, stream)
+             : launch_gemm_t<false, 128, false>(ta, tb, tc, a, grid, stream);
 }
 
 }  // namespace

@@ -13,17 +13,18 @@
 // art, replaced by):
 //   warp 0       TMA producer: one 128x128 A tile + one 256x128 B tile per
 //                K-block into a kStages-deep ring of 128B-swizzled smem.
-//   warp 1       TMEM owner + single-thread MMA issuer: per K-block four
-//                tcgen05.mma.kind::f8f6f4 (128x256x32) into a FRESH TMEM
-//                partial (the first with accumulate off).  Two partial
-//                buffers (2 x 256 FP32 columns = all 512) alternate, so the
-//                MMAs of block kb+1 overlap the promotion of block kb.
+//   warps 1-3    MMA issuers (warp 1 also owns TMEM): per K-block one
+//                thread issues four tcgen05.mma.kind::f8f6f4 (128x256x32)
+//                into a FRESH TMEM partial (the first with accumulate off);
+//                the three warps take K-blocks in turn.  Two partial buffers
+//                (2 x 256 FP32 columns = all 512) alternate, so the MMAs of
+//                block kb+1 overlap the promotion of block kb.
 //   warps 4..11  promotion + epilogue: each thread owns one row and 128
 //                columns of the 128x256 tile in 128 FP32 registers; per
 //                K-block it tcgen05.ld's its slice of the partial, frees the
 //                buffer, and does acc = fma(P, sA*sB, acc).  At the end of
 //                a tile it rounds (BF16, RNE) or keeps FP32 and stores.
-// Warps 2-3 idle.  Registers: warpgroup 0 gives up all but 56 per thread
+// Registers: warpgroup 0 gives up all but 56 per thread
 // (setmaxnreg) so the two promotion warpgroups can hold 224 each: the
 // 384 x 168 registers of the launch are exactly 128 x 56 + 256 x 224.
 // The grid is persistent (one CTA per SM); tiles are striped over CTAs.
@@ -52,11 +53,18 @@ constexpr uint32_t kBBytes = kBN * kBK;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
 
+constexpr int kMmaWarps = 3;              // warps 1..3 take turns issuing the MMAs
+constexpr int kSbRing = 8;                // per-column B-scale slices in flight
+constexpr uint32_t kSbSlotBytes = kBN * 4;  // one K-block's scales of a 256-column tile
+
 // dynamic shared memory layout (offsets from a 1024-aligned base)
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-constexpr uint32_t kOffBar = kOffB + kStages * kBBytes;       // 12 mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 16 * 8;               // tmem base, abort flag
+constexpr uint32_t kChunkBytes = 32 * 32;      // epilogue chunk: 32 rows x 32 bytes
+constexpr uint32_t kOffSB = kOffB + kStages * kBBytes;        // per-column sB ring
+constexpr uint32_t kOffStage = kOffSB + kSbRing * kSbSlotBytes;  // epilogue staging, 2 chunks per warp
+constexpr uint32_t kOffBar = kOffStage + 8 * 2 * kChunkBytes;  // 34 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 48 * 8;               // tmem base, abort flag
 constexpr uint32_t kOffPref = kOffMisc + 16;                  // grouped: tile prefix [E+1]
 constexpr uint32_t kOffRowOff = kOffPref + 4 * (kMaxExperts + 1);  // grouped: row offsets [E+1]
 constexpr uint32_t kSmemDense = kOffPref + 1024;              // + alignment slack
@@ -120,7 +128,7 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs& a, const in
 template <bool kOutF32, int kSbGran, bool kGrouped>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -128,7 +136,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t bar_empty = bar_full + kStages * 8;    // [kStages]
   const uint32_t bar_tfull = bar_empty + kStages * 8;   // [2]
   const uint32_t bar_tempty = bar_tfull + 2 * 8;        // [2]
-  const uint32_t bar_drain = bar_tempty + 2 * 8;        // [1]
+  const uint32_t bar_drain = bar_tempty + 2 * 8;        // [kMmaWarps]
+  const uint32_t bar_sfull = bar_drain + kMmaWarps * 8;  // [kSbRing]
+  const uint32_t bar_sempty = bar_sfull + kSbRing * 8;  // [kSbRing]
+  const uint32_t bar_turn = bar_sempty + kSbRing * 8;   // [kMmaWarps]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* pref = reinterpret_cast<int*>(smem + kOffPref);
@@ -147,11 +158,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, 8);  // one arrive per promotion warp
     }
-    mbar_init(bar_drain, 1);
+    for (int w = 0; w < kMmaWarps; ++w) {
+      mbar_init(bar_drain + 8 * w, 1);
+      mbar_init(bar_turn + 8 * w, 1);  // arrived by the issuer of the previous K-block
+    }
+    for (int r = 0; r < kSbRing; ++r) {
+      mbar_init(bar_sfull + 8 * r, 1);
+      mbar_init(bar_sempty + 8 * r, 8);  // one arrive per promotion warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -202,17 +221,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, issued = 0;
+      uint32_t g = 0;  // K-blocks issued so far: position in the sB ring
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
+        // per-column B scales of this tile's columns (the tail tile of an N
+        // that is not a multiple of 256 has 128 columns)
+        const uint32_t sb_bytes = static_cast<uint32_t>(args.N - ti.n0 < kBN ? args.N - ti.n0 : kBN) * 4u;
         for (int64_t kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+          if constexpr (kSbGran == 1) {
+            const uint32_t slot = g % kSbRing, sph = (g / kSbRing) & 1u;
+            if (!mbar_wait(bar_sempty + 8 * slot, sph ^ 1u, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar_sfull + 8 * slot, sb_bytes);
+            bulk_load(sbase + kOffSB + slot * kSbSlotBytes, args.sB + kb * args.N + ti.n0, sb_bytes,
+                      bar_sfull + 8 * slot);
+          }
           mbar_arrive_expect_tx(bar_full + 8 * stage, kABytes + kBBytes);
           tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, static_cast<int32_t>(kb * kBK),
                       static_cast<int32_t>(ti.m0), bar_full + 8 * stage);
           tma_load_2d(sbase + kOffB + stage * kBBytes, &tmB, static_cast<int32_t>(kb * kBK), ti.b_row,
                       bar_full + 8 * stage);
           ++issued;
+          ++g;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -224,40 +255,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(bar_full + 8 * stage, phase) && globaltimer_ns() - t0 < 1000000ull) {}
         }
+        if constexpr (kSbGran == 1) {
+          for (uint32_t i = 0; i < kSbRing && i < g; ++i) {
+            const uint32_t u = g - 1 - i;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar_sfull + 8 * (u % kSbRing), (u / kSbRing) & 1u) &&
+                   globaltimer_ns() - t0 < 1000000ull) {}
+          }
+        }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= kMmaWarps) {
+    // ------------------------------------------------------------ MMA issuers
+    // K-block g of this CTA's sequence is issued by warp 1 + g % 3.  A
+    // thread whose tcgen05.mma waits for room in the tensor pipe holds up the
+    // other warps of its scheduler; rotating the issue over three schedulers
+    // spreads that cost instead of slowing one quarter of the promotion rows.
+    // The issuers still go strictly in K-block order: the issuer of g waits
+    // for its turn (bar_turn, arrived by the issuer of g-1) before it waits
+    // on the ring barriers, so no barrier is ever waited on more than one
+    // phase ahead.
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
+      const uint32_t w = static_cast<uint32_t>(warp - 1);
+      const int64_t local_tiles =
+          blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      const uint64_t total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
       bool ok = true, any = false;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        for (int64_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t adesc = smem_desc_k_sw128(sbase + kOffA + stage * kABytes);
-          const uint64_t bdesc = smem_desc_k_sw128(sbase + kOffB + stage * kBBytes);
-          const uint32_t d = tmem_base + buf * kBN;
-#pragma unroll
-          for (int k = 0; k < kBK / 32; ++k) {
-            // K-slice k of the 128-byte swizzled rows: +32 bytes = +2 in the
-            // descriptor's 16-byte address units
-            mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
-          }
-          any = true;
-          mma_commit(bar_empty + 8 * stage);
-          mma_commit(bar_tfull + 8 * buf);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
-          buf ^= 1u;
-          if (buf == 0) bphase ^= 1u;
+      uint32_t turn = 0;  // turns this thread has taken
+      for (uint64_t g = w; g < total; g += kMmaWarps, ++turn) {
+        if (g > 0) {
+          // phase index of this turn on bar_turn[w]: warp 1 takes g = 0 without waiting
+          const uint32_t ph = (turn - (w == 0 ? 1u : 0u)) & 1u;
+          if (!mbar_wait(bar_turn + 8 * w, ph, abort_flag)) { ok = false; break; }
         }
+        const uint32_t stage = static_cast<uint32_t>(g % kStages);
+        const uint32_t phase = static_cast<uint32_t>(g / kStages) & 1u;
+        const uint32_t buf = static_cast<uint32_t>(g & 1u);
+        const uint32_t bphase = static_cast<uint32_t>(g >> 1) & 1u;
+        if (!mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t adesc = smem_desc_k_sw128(sbase + kOffA + stage * kABytes);
+        const uint64_t bdesc = smem_desc_k_sw128(sbase + kOffB + stage * kBBytes);
+        const uint32_t d = tmem_base + buf * kBN;
+#pragma unroll
+        for (int k = 0; k < kBK / 32; ++k) {
+          // K-slice k of the 128-byte swizzled rows: +32 bytes = +2 in the
+          // descriptor's 16-byte address units
+          mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+        }
+        any = true;
+        mma_commit(bar_empty + 8 * stage);
+        mma_commit(bar_tfull + 8 * buf);
+        mbar_arrive(bar_turn + 8 * ((w + 1) % kMmaWarps));  // the next K-block's issuer may go
       }
       if (!ok && any) {
         // drain: wait (bounded) until every MMA this thread issued is done
-        mma_commit(bar_drain);
+        mma_commit(bar_drain + 8 * w);
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < 1000000ull) {}
+        while (!mbar_try_wait(bar_drain + 8 * w, 0) && globaltimer_ns() - t0 < 1000000ull) {}
       }
     }
   } else if (warp >= 4) {
@@ -268,6 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;  // tile-local row
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
     uint32_t buf = 0, bphase = 0;
+    uint32_t g = 0;  // K-blocks consumed so far: position in the sB ring
     bool ok = true;
     const float* __restrict__ sA = args.sA;
     const float* __restrict__ sB = args.sB;
@@ -277,20 +334,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = m < ti.row_end;
       const int64_t nh = ti.n0 + h * 128;  // first column of this thread's half
       const bool cols_ok = nh < args.N;
+      const float* sb_col = sB + ti.sb_off + (nh >> 7) * KB;  // 128x128 scales of this half, by kb
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
 
+      // scales are loaded one K-block ahead so their latency hides behind
+      // the current block's promotion
+      float sa_next = row_ok ? __ldg(sA + m) : 0.f;
+      float sb_next = 0.f;
+      if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col) : 0.f;
+
       for (int64_t kb = 0; kb < KB; ++kb) {
-        const float sa = row_ok ? __ldg(sA + kb * args.lds_a + m) : 0.f;
-        float sb = 0.f;
-        if constexpr (kSbGran == 128) {
-          if (cols_ok) sb = __ldg(sB + ti.sb_off + (nh >> 7) * KB + kb);
-        } else {
-          // warm L1 with the next K-block's per-column scales of this half
-          if (cols_ok && kb + 1 < KB) {
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(sB + (kb + 1) * args.N + nh + lane * 4));
-          }
+        const float sa = sa_next;
+        const float sb = sb_next;
+        if (kb + 1 < KB) {
+          sa_next = row_ok ? __ldg(sA + (kb + 1) * args.lds_a + m) : 0.f;
+          if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col + kb + 1) : 0.f;
+        }
+        const float4* sbs = nullptr;  // per-column B scales of this half (smem)
+        uint32_t slot = 0;
+        if constexpr (kSbGran == 1) {
+          slot = g % kSbRing;
+          if (!mbar_wait(bar_sfull + 8 * slot, (g / kSbRing) & 1u, abort_flag)) { ok = false; break; }
+          sbs = reinterpret_cast<const float4*>(smem + kOffSB + slot * kSbSlotBytes) + h * 32;
         }
         if (!mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag)) { ok = false; break; }
         __syncwarp();
@@ -298,52 +365,104 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t taddr = tmem_base + t_lane + buf * kBN + h * 128;
         const float scale = sa * sb;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t p[32];
-          tmem_ld_32x32b_x32(taddr + c4 * 32, p);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t p[64];
+          tmem_ld_32x32b_x64(taddr + c2 * 64, p);
           tmem_ld_wait();
-          if (c4 == 3) {
+          if (c2 == 1) {
             // the whole partial of this warp is in registers: free the buffer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
           }
+          // acc += P * scale, two columns per packed FP32 instruction
           if constexpr (kSbGran == 128) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[c4 * 32 + j] = fmaf(__uint_as_float(p[j]), scale, acc[c4 * 32 + j]);
+            for (int j = 0; j < 64; j += 2)
+              fma2(acc[c2 * 64 + j], acc[c2 * 64 + j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), scale,
+                   scale);
           } else {
-            const float4* sbv = reinterpret_cast<const float4*>(sB + kb * args.N + nh + c4 * 32);
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 b4 = cols_ok ? __ldg(sbv + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
-              acc[c4 * 32 + 4 * j4 + 0] = fmaf(__uint_as_float(p[4 * j4 + 0]) * b4.x, sa, acc[c4 * 32 + 4 * j4 + 0]);
-              acc[c4 * 32 + 4 * j4 + 1] = fmaf(__uint_as_float(p[4 * j4 + 1]) * b4.y, sa, acc[c4 * 32 + 4 * j4 + 1]);
-              acc[c4 * 32 + 4 * j4 + 2] = fmaf(__uint_as_float(p[4 * j4 + 2]) * b4.z, sa, acc[c4 * 32 + 4 * j4 + 2]);
-              acc[c4 * 32 + 4 * j4 + 3] = fmaf(__uint_as_float(p[4 * j4 + 3]) * b4.w, sa, acc[c4 * 32 + 4 * j4 + 3]);
+            for (int j4 = 0; j4 < 16; ++j4) {
+              const float4 b4 = sbs[c2 * 16 + j4];
+              float* a = acc + c2 * 64 + 4 * j4;
+              float t0, t1, t2, t3;
+              mul2(t0, t1, __uint_as_float(p[4 * j4 + 0]), __uint_as_float(p[4 * j4 + 1]), b4.x, b4.y);
+              mul2(t2, t3, __uint_as_float(p[4 * j4 + 2]), __uint_as_float(p[4 * j4 + 3]), b4.z, b4.w);
+              fma2(a[0], a[1], t0, t1, sa, sa);
+              fma2(a[2], a[3], t2, t3, sa, sa);
             }
           }
         }
+        if constexpr (kSbGran == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sempty + 8 * slot);
+        }
+        ++g;
         buf ^= 1u;
         if (buf == 0) bphase ^= 1u;
       }
       if (!ok) break;
 
-      // ---- epilogue: this thread's row, 128 columns ----
-      if (row_ok && cols_ok) {
-        if constexpr (kOutF32) {
-          float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.C) + m * args.N + nh);
+      // ---- epilogue: this warp's 32 rows x 128 columns ----
+      // Whole-warp row blocks go out through shared memory and TMA stores in
+      // 32-row x 32-byte chunks (two chunk buffers per warp, so the write of
+      // one chunk overlaps the store of the previous); TMA clips rows past
+      // the end of C.  A grouped tile whose expert ends inside this warp's
+      // rows (the next expert's rows follow) stores its valid rows directly.
+      const int64_t wrow0 = ti.m0 + q * 32;
+      const bool via_tma = ti.row_end >= args.M || wrow0 + 32 <= ti.row_end;
+      if (cols_ok && wrow0 < ti.row_end) {
+        if (via_tma) {
+          uint8_t* stg = smem + kOffStage + (warp - 4) * 2 * kChunkBytes;
+          constexpr int kCols = kOutF32 ? 8 : 16;  // columns per 32-byte chunk row
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            out[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-        } else {
-          uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.N + nh);
+          for (int c = 0; c < 128 / kCols; ++c) {
+            uint8_t* cb = stg + (c & 1) * kChunkBytes;
+            if (lane == 0) bulk_wait_read<1>();  // the chunk buffer's previous store has read it
+            __syncwarp();
+            uint4 v0, v1;
+            if constexpr (kOutF32) {
+              v0 = make_uint4(__float_as_uint(acc[8 * c + 0]), __float_as_uint(acc[8 * c + 1]),
+                              __float_as_uint(acc[8 * c + 2]), __float_as_uint(acc[8 * c + 3]));
+              v1 = make_uint4(__float_as_uint(acc[8 * c + 4]), __float_as_uint(acc[8 * c + 5]),
+                              __float_as_uint(acc[8 * c + 6]), __float_as_uint(acc[8 * c + 7]));
+            } else {
+              v0 = make_uint4(cvt_bf16x2(acc[16 * c + 0], acc[16 * c + 1]), cvt_bf16x2(acc[16 * c + 2], acc[16 * c + 3]),
+                              cvt_bf16x2(acc[16 * c + 4], acc[16 * c + 5]), cvt_bf16x2(acc[16 * c + 6], acc[16 * c + 7]));
+              v1 = make_uint4(cvt_bf16x2(acc[16 * c + 8], acc[16 * c + 9]),
+                              cvt_bf16x2(acc[16 * c + 10], acc[16 * c + 11]),
+                              cvt_bf16x2(acc[16 * c + 12], acc[16 * c + 13]),
+                              cvt_bf16x2(acc[16 * c + 14], acc[16 * c + 15]));
+            }
+            *reinterpret_cast<uint4*>(cb + lane * 32) = v0;
+            *reinterpret_cast<uint4*>(cb + lane * 32 + 16) = v1;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, smem_u32(cb), static_cast<int32_t>(nh + c * kCols), static_cast<int32_t>(wrow0));
+              bulk_commit();
+            }
+          }
+        } else if (row_ok) {
+          if constexpr (kOutF32) {
+            float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.C) + m * args.N + nh);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            out[j] = make_uint4(cvt_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), cvt_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
-                                cvt_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), cvt_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+            for (int j = 0; j < 32; ++j)
+              out[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+          } else {
+            uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.N + nh);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              out[j] = make_uint4(cvt_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), cvt_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                                  cvt_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), cvt_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+          }
         }
       }
     }
+    // every TMA store of this warp has completed before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown

@@ -92,39 +92,34 @@ __device__ __forceinline__ void group_scale(float amax, float& s, float& inv) {
   inv = __fdiv_rn(448.0f, a);
 }
 
+// Shared-memory scratch of one tile's column / block reductions.
+struct QuantRed {
+  float red[4][128];  // per-warp column maxima
+  float inv[128];     // per-column inverse scales
+  float blk[4];       // per-warp block maxima
+};
+
+// Everything after the load: group amax, scales, E4M3 casts and stores of
+// the 128 x 128 tile (kb, mb) whose fragment this thread holds in `f`.
+// Called by all 128 threads of the CTA (it synchronizes the CTA).
 template <bool kF32, int kMode>
-__global__ void __launch_bounds__(128) quant_tile_kernel(const QuantArgs args) {
+__device__ __forceinline__ void quant_tile_body(const Frag<kF32>& f, const QuantArgs& args, int64_t kb, int64_t mb,
+                                                QuantRed& sm) {
   constexpr bool kRow = (kMode & kQRow) != 0;
   constexpr bool kCol = (kMode & kQCol) != 0;
   constexpr bool kBlk = (kMode & (kQBlk | kQBlkT)) != 0;
-
-  __shared__ float s_red[4][128];  // per-warp column maxima
-  __shared__ float s_inv[128];     // per-column inverse scales
-  __shared__ float s_blkred[4];
+  float (&s_red)[4][128] = sm.red;
+  float (&s_inv)[128] = sm.inv;
+  float (&s_blkred)[4] = sm.blk;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int c = lane & 15;  // column chunk: tile columns c*8 .. c*8+7
   const int g = lane >> 4;  // row half: tile rows warp*32 + g*16 + j
   const int64_t K = args.K;
-  const int64_t kb = blockIdx.x;
-  const int64_t mb = blockIdx.y;
   const int64_t k0 = kb * 128;
   const int64_t m0 = mb * 128;
   const int rbase = warp * 32 + g * 16;  // tile-local first row of this thread
-
-  // ---- load 16 rows x 8 columns ------------------------------------------
-  Frag<kF32> f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t m = m0 + rbase + j;
-    if (m < args.M) {
-      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
-      f.load(args.x, src * K + k0 + c * 8, j);
-    } else {
-      f.zero(j);
-    }
-  }
 
   // ---- 1x128 row groups ----------------------------------------------------
   if constexpr (kRow) {
@@ -233,6 +228,134 @@ __global__ void __launch_bounds__(128) quant_tile_kernel(const QuantArgs args) {
         *reinterpret_cast<uint4*>(args.q_blkT + (k0 + c * 8 + i) * ldT + m0 + rbase) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
+    }
+  }
+}
+
+// One CTA per 128 x 128 tile (grid: K/128 x ceil(M/128)); each thread loads
+// its 16 rows x 8 columns straight from global memory.  Used for FP32 input.
+template <bool kF32, int kMode>
+__global__ void __launch_bounds__(128) quant_tile_kernel(const QuantArgs args) {
+  __shared__ QuantRed sm;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 15;
+  const int g = lane >> 4;
+  const int64_t K = args.K;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int rbase = warp * 32 + g * 16;
+  Frag<kF32> f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + rbase + j;
+    if (m < args.M) {
+      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
+      f.load(args.x, src * K + k0 + c * 8, j);
+    } else {
+      f.zero(j);
+    }
+  }
+  quant_tile_body<kF32, kMode>(f, args, blockIdx.x, blockIdx.y, sm);
+}
+
+// Persistent BF16 quantizer.  Each CTA walks tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (t -> kb = t % (K/128), mb = t / (K/128)) and
+// keeps two tiles in flight: while it casts tile i from registers, tile i+1
+// and, once the registers are filled, tile i+2 stream into a double-buffered
+// shared-memory ring by bulk copies (one 256-byte row per thread, through an
+// optional row gather).  Every thread reads its fragment out of shared
+// memory (16-byte reads, two full rows per warp instruction: no bank
+// conflicts).  Waits are bounded: a copy that never lands sets the status
+// word, and the CTA drains what it issued and returns.
+constexpr int kPipeTileBytes = 128 * 256;  // 128 rows x 128 BF16
+
+// CTAs per SM the register budget is sized for: the two-output modes (row
+// and transposed column groups, or a block with its transpose) keep more
+// values live and get 2 CTAs of up to 255 registers; the others get 3.
+constexpr int quant_pipe_min_blocks(int mode) {
+  return (mode == (kQRow | kQCol) || mode == (kQBlk | kQBlkT)) ? 2 : 3;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
+    quant_pipe_kernel(const QuantArgs args, int64_t num_tiles) {
+  extern __shared__ __align__(128) uint8_t qsm[];  // [2][128 rows][256 bytes]
+  __shared__ QuantRed sm;
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = lane & 15;
+  const int g = lane >> 4;
+  const int rbase = warp * 32 + g * 16;
+  const int64_t K = args.K;
+  const int64_t kbt = K >> 7;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  const uint32_t buf0 = smem_u32(qsm);
+
+  // bytes that land in the buffer for tile tt (rows past M are not copied)
+  auto tile_bytes = [&](int64_t tt) -> uint32_t {
+    const int64_t rows = args.M - (tt / kbt) * 128;
+    return static_cast<uint32_t>(rows < 128 ? rows : 128) * 256u;
+  };
+  // this thread's row copy of tile tt into buffer b
+  auto issue_row = [&](int64_t tt, int b) {
+    const int64_t m = (tt / kbt) * 128 + tid;
+    if (m < args.M) {
+      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
+      bulk_load(buf0 + b * kPipeTileBytes + tid * 256,
+                static_cast<const uint16_t*>(args.x) + src * K + (tt % kbt) * 128, 256u, bar0 + 8 * b);
+    }
+  };
+
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t t0 = blockIdx.x, t1 = blockIdx.x + gridDim.x;
+  if (tid == 0) {
+    if (t0 < num_tiles) mbar_arrive_expect_tx(bar0, tile_bytes(t0));
+    if (t1 < num_tiles) mbar_arrive_expect_tx(bar0 + 8, tile_bytes(t1));
+  }
+  __syncthreads();
+  if (t0 < num_tiles) issue_row(t0, 0);
+  if (t1 < num_tiles) issue_row(t1, 1);
+
+  uint32_t it = 0;
+  int64_t t = t0;
+  for (; t < num_tiles; t += gridDim.x, ++it) {
+    const int b = it & 1;
+    const bool ok = mbar_wait(bar0 + 8 * b, (it >> 1) & 1u, abort_flag);
+    Frag<false> f;
+    if (ok) {
+      const uint8_t* tile = qsm + b * kPipeTileBytes;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) f.v[j] = *reinterpret_cast<const uint4*>(tile + (rbase + j) * 256 + c * 16);
+    }
+    const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
+    if (ok && tid == 0 && tn < num_tiles) mbar_arrive_expect_tx(bar0 + 8 * b, tile_bytes(tn));
+    // every thread has its fragment (buffer b is free) or some wait failed
+    if (__syncthreads_or(!ok)) break;
+    if (tn < num_tiles) issue_row(tn, b);
+    // rows past M were not copied: their registers hold stale data, but
+    // quant_tile_body neither stores nor reduces rows >= M
+    quant_tile_body<false, kMode>(f, args, t % kbt, t / kbt, sm);
+  }
+  if (t < num_tiles) {
+    // a wait failed: let every copy this CTA issued land before it exits
+    // (bounded; the status word already records the timeout)
+    for (uint32_t d = 0; d < 2; ++d) {
+      const uint32_t u = it + d;  // iteration whose copy may be in flight
+      if (t + static_cast<int64_t>(d) * gridDim.x >= num_tiles) break;
+      const uint64_t s0 = globaltimer_ns();
+      while (!mbar_try_wait(bar0 + 8 * (u & 1u), (u >> 1) & 1u) && globaltimer_ns() - s0 < 1000000ull) {}
     }
   }
 }
