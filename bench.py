@@ -454,13 +454,21 @@ def oracle_fprop_sample(xb, wb, R, C):
 
 
 def oracle_sample_size(xb, wb, seconds):
-    """(R, C) whose oracle_fprop_sample takes about `seconds`, calibrated on
-    a small slice; R rows of X and C (a multiple of 128) output columns."""
+    """(R, C) whose oracle_fprop_sample takes about `seconds`: R rows of X and
+    C (a multiple of 128) output columns.  The GEMM dominates the fprop step
+    at full size, so the sample keeps C small (weight quantization is a small
+    share) and grows R first; two calibration runs fit
+    t(R, 128) = fixed + R * per_row."""
     M, N = FPROP["M"], FPROP["N"]
-    dt, _ = oracle_fprop_sample(xb, wb, 4, 512)
-    scale = max(seconds / max(dt, 1e-4), 1e-3)
-    C = int(min(N, max(128, 512 * min(scale, N / 512.0)) // 128 * 128))
-    R = int(min(M, max(1, round(4 * scale * 512.0 / C))))
+    r1, r2 = 32, 128
+    t1, _ = oracle_fprop_sample(xb, wb, r1, 128)
+    t2, _ = oracle_fprop_sample(xb, wb, r2, 128)
+    per_row = max((t2 - t1) / (r2 - r1), 1e-7)
+    fixed = max(t1 - r1 * per_row, 0.0)
+    R = int(min(M, max(1, (seconds - fixed) / per_row)))
+    C = 128
+    if R == M:
+        C = int(min(N, max(128, 128 * (seconds // (fixed + M * per_row)))))
     return R, C
 
 
@@ -507,7 +515,7 @@ def reference_arm(args):
     import oracle
     import synth
     M, N, K = FPROP["M"], FPROP["N"], FPROP["K"]
-    X, W = synth.fprop_inputs(device="cpu", seed=2, M=64, N=N, K=K)
+    X, W = synth.fprop_inputs(device="cpu", seed=2, M=M, N=N, K=K)
     xb, wb = synth.bf16_bits(X), synth.bf16_bits(W)
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
     R, C = oracle_sample_size(xb, wb, per_step)
