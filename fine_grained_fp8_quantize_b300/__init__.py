@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "Fp8qError", "lib_path", "FP8Q_BF16", "FP8Q_FP32",
     "fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
-    "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_grouped_gemm",
+    "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_workspace_size",
+    "fp8q_grouped_gemm", "gemm_workspace",
     "fp8q_get_device_status", "fp8q_status_string", "fp8q_version",
     "quantize_act", "quantize_act_gather", "quantize_weight", "gemm", "grouped_gemm",
 ]
@@ -52,12 +53,15 @@ def _load():
     L.fp8q_quantize_weight_ex.argtypes = [P, I32, I64, I64, P, P, P, P, P]
     L.fp8q_gemm.argtypes = [P, P, P, P, P, I64, I64, I64, I32, P]
     L.fp8q_gemm_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I32, P]
+    L.fp8q_gemm_ws.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I32, P, ctypes.c_size_t, P]
+    L.fp8q_gemm_workspace_size.argtypes = []
+    L.fp8q_gemm_workspace_size.restype = ctypes.c_size_t
     L.fp8q_grouped_gemm.argtypes = [P, P, P, P, P, P, ctypes.c_int32, I64, I64, I64, I32, P]
     L.fp8q_get_device_status.argtypes = [P]
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [I32]
     for name in ("fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
-                 "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_grouped_gemm",
+                 "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_grouped_gemm",
                  "fp8q_get_device_status", "fp8q_version"):
         getattr(L, name).restype = I32
     return L
@@ -163,6 +167,20 @@ def fp8q_gemm_ex(Aq, sA, Bq, sB, C, sb_gran_n, stream=None):
         _stream(stream)))
 
 
+def fp8q_gemm_workspace_size():
+    return int(_lib.fp8q_gemm_workspace_size())
+
+
+def fp8q_gemm_ws(Aq, sA, Bq, sB, C, sb_gran_n, workspace, stream=None):
+    _contig(Aq, sA, Bq, sB, C, workspace)
+    M, K = Aq.shape
+    N = Bq.shape[0]
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("fp8q_gemm_ws", _lib.fp8q_gemm_ws(
+        _ptr(Aq), _ptr(sA), _ptr(Bq), _ptr(sB), _ptr(C), M, N, K, _out_dtype(C), int(sb_gran_n),
+        _ptr(workspace), nbytes, _stream(stream)))
+
+
 def fp8q_grouped_gemm(Aq, sA, Bq, sB, C, row_offsets, stream=None):
     _contig(Aq, sA, Bq, sB, C, row_offsets)
     if row_offsets.dtype != torch.int32:
@@ -218,11 +236,21 @@ def quantize_weight(w, transposed=False, stream=None):
     return q, s, q_t, s_t
 
 
-def gemm(Aq, sA, Bq, sB, out_dtype=torch.bfloat16, sb_gran_n=128, stream=None):
+def gemm_workspace(device=None):
+    """A zero-filled stream-K workspace for fp8q_gemm_ws on `device`."""
+    n = fp8q_gemm_workspace_size()
+    if n == 0:
+        raise Fp8qError("fp8q_gemm_workspace_size", 5)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gemm(Aq, sA, Bq, sB, out_dtype=torch.bfloat16, sb_gran_n=128, workspace=None, stream=None):
     M = Aq.shape[0]
     N = Bq.shape[0]
     C = torch.empty(M, N, dtype=out_dtype, device=Aq.device)
-    if sb_gran_n == 128:
+    if workspace is not None:
+        fp8q_gemm_ws(Aq, sA, Bq, sB, C, sb_gran_n, workspace, stream)
+    elif sb_gran_n == 128:
         fp8q_gemm(Aq, sA, Bq, sB, C, stream)
     else:
         fp8q_gemm_ex(Aq, sA, Bq, sB, C, sb_gran_n, stream)

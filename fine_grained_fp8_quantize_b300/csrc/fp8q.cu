@@ -154,21 +154,59 @@ int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cu
   return launch_quant_pipe<kMode>(a, gx * gy, s);
 }
 
-template <bool kOutF32, int kSbGran, bool kGrouped>
-int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
+// One CTA per SM (persistent).  A stream-K launch is cooperative: its CTAs
+// wait on each other's partial tiles, so they must all be resident at once.
+template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK>
+int launch_gemm_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
                   cudaStream_t s) {
-  auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped>;
+  auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped, kStreamK>;
   const uint32_t smem = kGrouped ? kSmemGrouped : kSmemDense;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return FP8Q_ERR_CUDA;
-  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, tc, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.streamk ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a) != cudaSuccess) return FP8Q_ERR_CUDA;
   return launch_status();
+}
+
+template <bool kOutF32, int kSbGran, bool kGrouped>
+int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
+                  cudaStream_t s) {
+  if constexpr (kGrouped) {
+    return launch_gemm_k<kOutF32, kSbGran, true, false>(ta, tb, tc, a, grid, s);
+  } else {
+    return a.streamk ? launch_gemm_k<kOutF32, kSbGran, false, true>(ta, tb, tc, a, grid, s)
+                     : launch_gemm_k<kOutF32, kSbGran, false, false>(ta, tb, tc, a, grid, s);
+  }
+}
+
+// Stream-K workspace: [flags: one u32 per CTA, padded to 256 bytes]
+// [partial tiles: one 128 x 256 FP32 tile per CTA].
+constexpr size_t kPartialBytes = static_cast<size_t>(kBM) * kBN * 4;
+size_t workspace_bytes_for(int ctas) {
+  return ((static_cast<size_t>(ctas) * 4 + 255) & ~size_t(255)) + static_cast<size_t>(ctas) * kPartialBytes;
+}
+
+// Call epochs for the stream-K flags: never 0 (the idle value).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
 }
 
 int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C, int64_t M,
                 int64_t N, int64_t K, int out_dtype, int sb_gran, const int32_t* row_offsets, int32_t E,
-                cudaStream_t stream) {
+                cudaStream_t stream, void* workspace = nullptr, size_t workspace_bytes = 0) {
   const bool grouped = row_offsets != nullptr;
   if (out_dtype != FP8Q_BF16 && out_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
   if (sb_gran != 128 && sb_gran != 1) return FP8Q_ERR_DTYPE;
@@ -180,7 +218,7 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   if (M == 0) return FP8Q_OK;  // empty operands may carry null pointers
   if (!Aq || !sA || !Bq || !sB || !C) return FP8Q_ERR_NULL;
   if (!aligned16(Aq) || !aligned16(sA) || !aligned16(Bq) || !aligned16(sB) || !aligned16(C) ||
-      (grouped && !aligned16(row_offsets)))
+      (grouped && !aligned16(row_offsets)) || (workspace && !aligned16(workspace)))
     return FP8Q_ERR_ALIGN;
   DeviceInfo di;
   int st = check_device(&di);
@@ -206,6 +244,10 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   a.tiles_n = static_cast<int>((N + kBN - 1) / kBN);
   a.row_offsets = row_offsets;
   a.E = grouped ? E : 1;
+  a.streamk = 0;
+  a.ws = nullptr;
+  a.flags = nullptr;
+  a.epoch = 0;
 
   int64_t tiles_upper;
   if (grouped) {
@@ -214,7 +256,23 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
     tiles_upper = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   }
   if (tiles_upper > (int64_t(1) << 31) - 1) return FP8Q_ERR_SHAPE;
-  const int grid = static_cast<int>(tiles_upper < di.sms ? tiles_upper : di.sms);
+  int grid = static_cast<int>(tiles_upper < di.sms ? tiles_upper : di.sms);
+  if (workspace != nullptr && !grouped) {
+    if (workspace_bytes < workspace_bytes_for(di.sms)) return FP8Q_ERR_WORKSPACE;
+    // stream-K when whole tiles leave the last wave of the persistent grid
+    // less than 95% busy (or there are fewer tiles than SMs)
+    const int64_t waves = (tiles_upper + di.sms - 1) / di.sms;
+    const int64_t kb_total = tiles_upper * (K / kBK);
+    if (tiles_upper * 100 < waves * di.sms * 95 && kb_total >= di.sms &&
+        kb_total < (int64_t(1) << 62) / di.sms) {
+      grid = di.sms;
+      a.streamk = 1;
+      a.flags = static_cast<uint32_t*>(workspace);
+      a.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) +
+                                       ((static_cast<size_t>(di.sms) * 4 + 255) & ~size_t(255)));
+      a.epoch = next_epoch();
+    }
+  }
   const bool f32 = out_dtype == FP8Q_FP32;
   if (grouped) {
     return f32 ? launch_gemm_t<true, 128, true>(ta, tb, tc, a, grid, stream)
@@ -244,6 +302,7 @@ const char* fp8q_status_string(int status) {
     case FP8Q_ERR_DEVICE: return "current device is not sm_103 (B300)";
     case FP8Q_ERR_CUDA: return "CUDA call or kernel launch failed";
     case FP8Q_ERR_TIMEOUT: return "a kernel pipeline wait timed out on the device";
+    case FP8Q_ERR_WORKSPACE: return "workspace smaller than fp8q_gemm_workspace_size()";
     default: return "unknown status";
   }
 }
@@ -345,6 +404,19 @@ int fp8q_gemm_ex(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const fl
                  int64_t N, int64_t K, int out_dtype, int sb_gran_n, fp8q_stream_t stream) {
   return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fp8q_gemm_workspace_size(void) {
+  DeviceInfo di;
+  if (check_device(&di) != FP8Q_OK) return 0;
+  return workspace_bytes_for(di.sms);
+}
+
+int fp8q_gemm_ws(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C, int64_t M,
+                 int64_t N, int64_t K, int out_dtype, int sb_gran_n, void* workspace, size_t workspace_bytes,
+                 fp8q_stream_t stream) {
+  return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0,
+                     reinterpret_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
 int fp8q_grouped_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C,

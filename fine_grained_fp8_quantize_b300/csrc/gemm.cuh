@@ -82,7 +82,22 @@ struct GemmArgs {
   int tiles_n;
   const int32_t* row_offsets;  // grouped [E+1]
   int E;
+  // stream-K (dense only, kernel variant kStreamK): each CTA takes an equal
+  // share of the tile-major sequence of all tiles' K-blocks; a tile split
+  // between CTAs is finished by the CTA holding its first K-blocks, which
+  // adds the other CTAs' FP32 partial tiles (ws, slot = CTA index) once
+  // their flags carry this call's epoch.
+  int streamk;
+  float4* ws;        // [gridDim.x][2 halves][32 column quads][128 rows] float4
+  uint32_t* flags;   // [gridDim.x], zero between calls
+  uint32_t epoch;    // nonzero, distinct from the previous call's
 };
+
+// First K-block of CTA `cta` of `grid` in the stream-K split of `total`
+// K-blocks (CTA c takes [begin(c), begin(c+1))).
+__device__ __forceinline__ int64_t streamk_begin(int64_t total, int64_t cta, int64_t grid) {
+  return total * cta / grid;
+}
 
 struct TileInfo {
   int64_t m0;       // first row (global)
@@ -125,7 +140,7 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs& a, const in
   return ti;
 }
 
-template <bool kOutF32, int kSbGran, bool kGrouped>
+template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -223,12 +238,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t stage = 0, phase = 0, issued = 0;
       uint32_t g = 0;  // K-blocks issued so far: position in the sB ring
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      // K-blocks [kb_lo, kb_hi) of tile t
+      auto load_tile = [&](int t, int64_t kb_lo, int64_t kb_hi) {
         const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
         // per-column B scales of this tile's columns (the tail tile of an N
         // that is not a multiple of 256 has 128 columns)
         const uint32_t sb_bytes = static_cast<uint32_t>(args.N - ti.n0 < kBN ? args.N - ti.n0 : kBN) * 4u;
-        for (int64_t kb = 0; kb < KB; ++kb) {
+        for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (kSbGran == 1) {
             const uint32_t slot = g % kSbRing, sph = (g / kSbRing) & 1u;
@@ -245,6 +261,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++issued;
           ++g;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      };
+      if constexpr (!kStreamK) {
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) load_tile(t, 0, KB);
+      } else {
+        const int64_t all = static_cast<int64_t>(num_tiles) * KB;
+        const int64_t e = streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x);
+        for (int64_t it = streamk_begin(all, blockIdx.x, gridDim.x); ok && it < e;) {
+          const int t = static_cast<int>(it / KB);
+          const int64_t lo = it - static_cast<int64_t>(t) * KB;
+          const int64_t hi = e - static_cast<int64_t>(t) * KB < KB ? e - static_cast<int64_t>(t) * KB : KB;
+          load_tile(t, lo, hi);
+          it += hi - lo;
         }
       }
       if (!ok) {
@@ -277,9 +306,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // phase ahead.
     if (lane == 0) {
       const uint32_t w = static_cast<uint32_t>(warp - 1);
-      const int64_t local_tiles =
-          blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-      const uint64_t total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
+      uint64_t total;  // K-blocks of this CTA
+      if constexpr (kStreamK) {
+        const int64_t all = static_cast<int64_t>(num_tiles) * KB;
+        total = static_cast<uint64_t>(streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x) -
+                                      streamk_begin(all, blockIdx.x, gridDim.x));
+      } else {
+        const int64_t local_tiles =
+            blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
+      }
       bool ok = true, any = false;
       uint32_t turn = 0;  // turns this thread has taken
       for (uint64_t g = w; g < total; g += kMmaWarps, ++turn) {
@@ -328,7 +364,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     const float* __restrict__ sA = args.sA;
     const float* __restrict__ sB = args.sB;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    // K-blocks [kb_lo, kb_hi) of tile t: promotion, then the epilogue (whole
+    // tile, or the stream-K partial exchange)
+    auto tile_work = [&](int t, int64_t kb_lo, int64_t kb_hi) {
       const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
       const int64_t m = ti.m0 + row;
       const bool row_ok = m < ti.row_end;
@@ -341,14 +379,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       // scales are loaded one K-block ahead so their latency hides behind
       // the current block's promotion
-      float sa_next = row_ok ? __ldg(sA + m) : 0.f;
+      float sa_next = row_ok ? __ldg(sA + kb_lo * args.lds_a + m) : 0.f;
       float sb_next = 0.f;
-      if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col) : 0.f;
+      if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col + kb_lo) : 0.f;
 
-      for (int64_t kb = 0; kb < KB; ++kb) {
+      for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
         const float sa = sa_next;
         const float sb = sb_next;
-        if (kb + 1 < KB) {
+        if (kb + 1 < kb_hi) {
           sa_next = row_ok ? __ldg(sA + (kb + 1) * args.lds_a + m) : 0.f;
           if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col + kb + 1) : 0.f;
         }
@@ -402,7 +440,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         buf ^= 1u;
         if (buf == 0) bphase ^= 1u;
       }
-      if (!ok) break;
+      if constexpr (kStreamK) {
+        // the exchange below synchronizes the promotion warps: they all
+        // leave together if any of them gave up a wait
+        if (promo_bar_or(!ok)) {
+          ok = false;
+          return;
+        }
+        if (kb_lo > 0) {
+          // this CTA holds the later K-blocks of a split tile: leave the FP32
+          // partial in its workspace slot and raise its flag
+          float4* dst = args.ws + (static_cast<size_t>(blockIdx.x) * 2 + h) * 32 * 128 + row;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            dst[j * 128] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+          __threadfence();
+          promo_bar_sync();
+          if (warp == 4 && lane == 0) st_release_gpu(args.flags + blockIdx.x, args.epoch);
+          return;
+        }
+        if (kb_hi < KB) {
+          // this CTA holds the first K-blocks of a split tile: add the
+          // partials of the CTAs holding the rest, in CTA order
+          const int64_t all = static_cast<int64_t>(num_tiles) * KB;
+          const int64_t tile_end = static_cast<int64_t>(t + 1) * KB;
+          for (int64_t j = static_cast<int64_t>(blockIdx.x) + 1; j < gridDim.x; ++j) {
+            const int64_t bj = streamk_begin(all, j, gridDim.x);
+            if (bj >= tile_end) break;
+            if (streamk_begin(all, j + 1, gridDim.x) == bj) continue;  // CTA j has no K-blocks
+            if (warp == 4 && lane == 0) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_gpu(args.flags + j) != args.epoch) {
+                if (*abort_flag) break;
+                if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                  atomicCAS(&g_status_word, 0u, kStatusTimeout);
+                  *abort_flag = 1;
+                  break;
+                }
+                __nanosleep(64);
+              }
+            }
+            promo_bar_sync();
+            const float4* src = args.ws + (static_cast<size_t>(j) * 2 + h) * 32 * 128 + row;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const float4 v = __ldcg(src + jj * 128);
+              acc[4 * jj + 0] += v.x;
+              acc[4 * jj + 1] += v.y;
+              acc[4 * jj + 2] += v.z;
+              acc[4 * jj + 3] += v.w;
+            }
+            promo_bar_sync();  // every thread has read slot j: its flag may drop
+            if (warp == 4 && lane == 0) args.flags[j] = 0u;
+          }
+        }
+      } else {
+        if (!ok) return;
+      }
 
       // ---- epilogue: this warp's 32 rows x 128 columns ----
       // Whole-warp row blocks go out through shared memory and TMA stores in
@@ -458,6 +552,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                   cvt_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), cvt_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
           }
         }
+      }
+    };
+    if constexpr (!kStreamK) {
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) tile_work(t, 0, KB);
+    } else {
+      const int64_t all = static_cast<int64_t>(num_tiles) * KB;
+      const int64_t e = streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x);
+      for (int64_t it = streamk_begin(all, blockIdx.x, gridDim.x); ok && it < e;) {
+        const int t = static_cast<int>(it / KB);
+        const int64_t lo = it - static_cast<int64_t>(t) * KB;
+        const int64_t hi = e - static_cast<int64_t>(t) * KB < KB ? e - static_cast<int64_t>(t) * KB : KB;
+        tile_work(t, lo, hi);
+        it += hi - lo;
       }
     }
     // every TMA store of this warp has completed before the CTA exits

@@ -58,6 +58,7 @@
 #ifndef FP8Q_H
 #define FP8Q_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -82,7 +83,8 @@ typedef enum {
     FP8Q_ERR_DTYPE = 4,    /* unknown dtype / granularity code                */
     FP8Q_ERR_DEVICE = 5,   /* current device is not sm_103 (B300)             */
     FP8Q_ERR_CUDA = 6,     /* a CUDA call or launch failed                     */
-    FP8Q_ERR_TIMEOUT = 7   /* a kernel's pipeline wait timed out (device side) */
+    FP8Q_ERR_TIMEOUT = 7,  /* a kernel's pipeline wait timed out (device side) */
+    FP8Q_ERR_WORKSPACE = 8 /* workspace smaller than fp8q_gemm_workspace_size() */
 } fp8q_status;
 
 typedef enum {
@@ -179,6 +181,38 @@ FP8Q_API int fp8q_gemm(const uint8_t *Aq, const float *sA, const uint8_t *Bq, co
 FP8Q_API int fp8q_gemm_ex(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
                  void *C, int64_t M, int64_t N, int64_t K, int out_dtype,
                  int sb_gran_n, fp8q_stream_t stream);
+
+/*
+ * fp8q_gemm_workspace_size -- bytes of device workspace fp8q_gemm_ws needs on
+ * the current device (one flag word and one 128x256 FP32 partial tile per
+ * SM, about 19 MB on a B300), or 0 if the current device is not sm_103.
+ */
+FP8Q_API size_t fp8q_gemm_workspace_size(void);
+
+/*
+ * fp8q_gemm_ws -- fp8q_gemm_ex with a caller-owned device workspace that lets
+ * the persistent kernel balance its K loop across SMs ("stream-K").
+ *   workspace        device memory of at least fp8q_gemm_workspace_size()
+ *                    bytes, 16-byte aligned, ZERO-FILLED before its first use.
+ *                    Every call that completes leaves it zeroed again, so one
+ *                    allocation serves any number of calls on one stream.
+ *                    After a call that reported FP8Q_ERR_TIMEOUT, zero it
+ *                    again.  Calls sharing a workspace must not overlap on
+ *                    the GPU (use one stream, or one workspace per stream).
+ *   workspace_bytes  its size; smaller than required -> FP8Q_ERR_WORKSPACE.
+ * workspace == NULL runs exactly as fp8q_gemm_ex.  Otherwise, when whole
+ * 128x256 output tiles would leave the last wave of the one-CTA-per-SM grid
+ * less than 95% busy, every SM takes an equal share of the tile-major
+ * sequence of all tiles' 128-K blocks; a tile whose blocks are split between
+ * SMs is finished by the SM holding its first blocks, which adds the other
+ * SMs' FP32 partial tiles in SM order (deterministic).  The promotion every
+ * 128 K is unchanged; only where the FP32 sum of a tile is formed moves.
+ * Same layouts, accuracy and errors as fp8q_gemm_ex.
+ */
+FP8Q_API int fp8q_gemm_ws(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
+                 void *C, int64_t M, int64_t N, int64_t K, int out_dtype,
+                 int sb_gran_n, void *workspace, size_t workspace_bytes,
+                 fp8q_stream_t stream);
 
 /*
  * fp8q_grouped_gemm -- MoE grouped block-scaled FP8 GEMM over E experts with

@@ -42,8 +42,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     assert lib.fp8q_version() == 100
-    for code in range(8):
+    for code in range(9):
         assert lib.fp8q_status_string(code)
+    assert lib.fp8q_status_string(8) == b"workspace smaller than fp8q_gemm_workspace_size()"
     assert lib.fp8q_status_string(3) == b"pointer not 16-byte aligned"
 
 
@@ -64,6 +65,9 @@ def test_gemm_validation(lib):
     assert g(A, A, MIS, A, A, 128, 128, 128, 0, None) == 3           # alignment
     gx = lib.fp8q_gemm_ex
     assert gx(A, A, A, A, A, 128, 128, 128, 1, 64, None) == 4        # granularity
+    gw = lib.fp8q_gemm_ws
+    assert gw(A, A, A, A, A, 128, 100, 128, 0, 128, A, 1 << 30, None) == 2  # N % 128
+    assert gw(A, A, A, A, A, 128, 128, 128, 0, 128, MIS, 1 << 30, None) == 3  # workspace alignment
     gg = lib.fp8q_grouped_gemm
     assert gg(A, A, A, A, A, NULL, 4, 128, 128, 128, 0, None) == 1   # no offsets
     assert gg(A, A, A, A, A, A, 0, 128, 128, 128, 0, None) == 2      # E < 1

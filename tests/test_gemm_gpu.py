@@ -234,3 +234,71 @@ def test_moe_full_size_256_experts(f):
     rows = np.linspace(0, len(src) - 1, 64).astype(np.int64)
     oq, os_ = oracle.quantize_act_rows(host_bits(X[torch.from_numpy(src[rows]).cuda()]))
     assert np.array_equal(hqx[rows], oq) and np.array_equal(hsx[:, rows], os_)
+
+
+# ----------------------------------------------------------------- stream-K
+
+@pytest.fixture(scope="module")
+def workspace(f):
+    return f.gemm_workspace()
+
+
+def _flags_zero(f, ws):
+    # the flag words (one per SM, first bytes of the workspace) are back to 0
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    return bool((ws[:4 * n] == 0).all())
+
+
+@pytest.mark.parametrize("M,N,K,gran,out", [
+    (256, 512, 8192, 128, torch.float32),     # 4 tiles, 64 K-blocks each: every tile split ~37 ways
+    (1000, 1280, 4096, 128, torch.bfloat16),  # ragged rows, 40 tiles
+    (384, 768, 2048, 1, torch.float32),       # per-column B scales
+    (200, 384, 1024, 128, torch.bfloat16),    # N tail tile of 128 columns
+])
+def test_streamk_matches_oracle(f, workspace, M, N, K, gran, out):
+    rng = np.random.default_rng(M + N + K + gran)
+    Aq, Bq = rand_codes(rng, (M, K)), rand_codes(rng, (N, K))
+    sA = rand_scales(rng, (K // 128, M))
+    sB = rand_scales(rng, (N // 128, K // 128)) if gran == 128 else rand_scales(rng, (K // 128, N))
+    dA, dsA, dB, dsB = dev(Aq), dev(sA), dev(Bq), dev(sB)
+    C = f.gemm(dA, dsA, dB, dsB, out_dtype=out, sb_gran_n=gran, workspace=workspace)
+    torch.cuda.synchronize()
+    status_ok()
+    assert _flags_zero(f, workspace)
+    ex, ab, _ = oracle.gemm(Aq, sA, Bq, sB, sb_gran=gran)
+    check_gemm(gemm_out_to_f64(C), ex, ab, out == torch.bfloat16, "stream-K %dx%dx%d" % (M, N, K))
+    # deterministic: a second call gives the same bits
+    C2 = f.gemm(dA, dsA, dB, dsB, out_dtype=out, sb_gran_n=gran, workspace=workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16) if out == torch.bfloat16 else C.view(torch.int32),
+                       C2.view(torch.int16) if out == torch.bfloat16 else C2.view(torch.int32))
+
+
+def test_streamk_wgrad_full_size(f, workspace):
+    # Wgrad 2048x7168x8192: 448 tiles of 128x256 on the SMs (3.03 waves), the
+    # case the balanced split is for
+    dY, X = synth.wgrad_inputs(device="cuda")
+    _, _, qdy, sdy = f.quantize_act(dY, row=False, col=True)
+    _, _, qx, sx = f.quantize_act(X, row=False, col=True)
+    C = f.gemm(qdy, sdy, qx, sx, out_dtype=torch.float32, sb_gran_n=1, workspace=workspace)
+    C0 = f.gemm(qdy, sdy, qx, sx, out_dtype=torch.float32, sb_gran_n=1)
+    torch.cuda.synchronize()
+    status_ok()
+    assert _flags_zero(f, workspace)
+    mi, ni = sample_points(2048, 7168, seed=5)
+    ex, ab, _ = oracle.gemm_points(to_np(qdy), to_np(sdy), to_np(qx), to_np(sx), mi, ni, sb_gran=1)
+    check_gemm(gemm_out_to_f64(C)[mi, ni], ex, ab, False, "wgrad stream-K")
+    # and it agrees with the data-parallel schedule to FP32 summation order
+    d = (C - C0).abs().double().cpu().numpy()[mi, ni]
+    assert (d <= 1e-5 * ab + 1e-30).all()
+
+
+def test_workspace_too_small_is_rejected(f):
+    A = torch.zeros(128, 128, dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, 128, dtype=torch.float32, device="cuda")
+    sb = torch.ones(1, 1, dtype=torch.float32, device="cuda")
+    C = torch.empty(128, 128, dtype=torch.float32, device="cuda")
+    small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(f.Fp8qError) as e:
+        f.fp8q_gemm_ws(A, s, A, sb, C, 128, small)
+    assert e.value.status == 8
