@@ -288,6 +288,43 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Library-owned stream-K scratch for fp8q_gemm_ws_static.  For callers that
+// have no allocator at hand -- e.g. a plugin or operator interface whose
+// enqueue step is handed only its input and output buffers, or a path that
+// must not take cudaMalloc's implicit device-wide synchronization -- the
+// workspace fp8q_gemm_ws would need lives in this fixed array instead.  It is
+// sized for a grid of up to kStaticScratchCtas CTAs (one per SM), about
+// 20 MB, and every GPU that loads the library holds it until the process
+// exits.
+// ---------------------------------------------------------------------------
+constexpr int kStaticScratchCtas = 160;
+constexpr size_t kStaticScratchBytes = ((static_cast<size_t>(kStaticScratchCtas) * 4 + 255) & ~size_t(255)) +
+                                       static_cast<size_t>(kStaticScratchCtas) * (static_cast<size_t>(kBM) * kBN * 4);
+static __device__ __align__(256) unsigned char g_gemm_scratch[kStaticScratchBytes];
+
+namespace {
+
+// Device address of g_gemm_scratch on the current device.  In host code the
+// array's name is only a host-side handle, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gemm_scratch) != cudaSuccess || p == nullptr) return FP8Q_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return FP8Q_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp8q_version(void) { return kVersion; }
@@ -417,6 +454,23 @@ int fp8q_gemm_ws(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const fl
                  fp8q_stream_t stream) {
   return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0,
                      reinterpret_cast<cudaStream_t>(stream), workspace, workspace_bytes);
+}
+
+int fp8q_gemm_ws_static(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C,
+                        int64_t M, int64_t N, int64_t K, int out_dtype, int sb_gran_n, fp8q_stream_t stream) {
+  DeviceInfo di;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  // the grid (one CTA per SM) must fit the fixed scratch
+  if (workspace_bytes_for(di.sms) > kStaticScratchBytes) return FP8Q_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int sst = static_scratch(&scratch);
+  if (sst != FP8Q_OK) return sst;
+  // the flag words must start at zero; clear them on this stream (earlier
+  // calls leave them zero unless one stopped on a timeout)
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(di.sms) * 4, cs) != cudaSuccess) return FP8Q_ERR_CUDA;
+  return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0, cs, scratch, kStaticScratchBytes);
 }
 
 int fp8q_grouped_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C,

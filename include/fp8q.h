@@ -215,6 +215,31 @@ FP8Q_API int fp8q_gemm_ws(const uint8_t *Aq, const float *sA, const uint8_t *Bq,
                  fp8q_stream_t stream);
 
 /*
+ * fp8q_gemm_ws_static -- fp8q_gemm_ws that allocates nothing and takes no
+ * workspace: the stream-K scratch is a fixed array inside the library.
+ * (The pages have no counterpart to this; it exists for callers that cannot
+ * allocate device memory -- e.g. a plugin or operator interface whose
+ * enqueue step is handed only its input and output buffers, or a path that
+ * must not take cudaMalloc's implicit device-wide synchronization.)
+ *  - The array holds the workspace of a grid of up to 160 CTAs (one per SM;
+ *    about 20 MB) and stays resident on every GPU that loads the library
+ *    until the process exits.  A device with more SMs than that gets
+ *    FP8Q_ERR_WORKSPACE.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and leaves its contents for the next;
+ *    each call first clears the flag words on its stream (a small memset).
+ *    Calls whose kernels overlap on the GPU race on the array: keep them on
+ *    one stream, or use fp8q_gemm_ws with a workspace per stream.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments, layouts, accuracy and errors as fp8q_gemm_ex.
+ */
+FP8Q_API int fp8q_gemm_ws_static(const uint8_t *Aq, const float *sA, const uint8_t *Bq, const float *sB,
+                        void *C, int64_t M, int64_t N, int64_t K, int out_dtype,
+                        int sb_gran_n, fp8q_stream_t stream);
+
+/*
  * fp8q_grouped_gemm -- MoE grouped block-scaled FP8 GEMM over E experts with
  * ragged rows (no token dropping).
  *   Aq           [total_rows][K] codes of the dispatched (expert-grouped) rows.
