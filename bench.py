@@ -55,7 +55,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
-    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe"],
+    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum"],
                    help="all: the Fprop step plus the breakdown; else time one workload alone")
     p.add_argument("--no-breakdown", action="store_true", help="time the Fprop step only")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
@@ -436,9 +436,49 @@ def case_moe(args, f, torch, synth, pk, iters):
             "roofline": tensor_roofline("gemm_kernel<bf16 out, grouped>", fl, ms_g, pk, "moe_256x2048x7168")}
 
 
+def case_accum(args, f, torch, synth, pk, iters):
+    """Accumulation precision at K = 4096 (the pages' example): the block-scaled
+    GEMM promoting every 128 K versus the whole K accumulated inside the tensor
+    core (fp8q_gemm_unpromoted), both on the same E4M3 codes with unit scales,
+    against the exact FP64 result on 8192 sampled outputs."""
+    import oracle
+    M = N = 1024
+    K = 4096
+    out = {}
+    for name, absval in (("signed N(0,1) codes", False), ("positive |N(0,1)| codes", True)):
+        A = synth.matrix(11, 1, M, K, 1.0, dtype=torch.float32, device="cuda")
+        B = synth.matrix(11, 2, N, K, 1.0, dtype=torch.float32, device="cuda")
+        if absval:
+            A, B = A.abs(), B.abs()
+        qa, _, _, _ = f.quantize_act(A)
+        qb, _, _, _ = f.quantize_act(B)
+        ones_a = torch.ones(K // 128, M, device="cuda")
+        ones_b = torch.ones(N // 128, K // 128, device="cuda")
+        Cp = f.gemm(qa, ones_a, qb, ones_b, out_dtype=torch.float32)
+        Cu = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        f.fp8q_gemm_unpromoted(qa, qb, Cu)
+        torch.cuda.synchronize()
+        check_status(f, "after the accumulation study")
+        rng = np.random.default_rng(0)
+        mi = rng.integers(0, M, 8192)
+        ni = rng.integers(0, N, 8192)
+        ex, ab, _ = oracle.gemm_points(qa.cpu().numpy(), ones_a.cpu().numpy(), qb.cpu().numpy(),
+                                       ones_b.cpu().numpy(), mi, ni)
+        big = np.abs(ex) >= 1e-3 * np.abs(ex).max()
+        res = {}
+        for label, C in (("promoted every 128", Cp), ("unpromoted", Cu)):
+            c = C.double().cpu().numpy()[mi, ni]
+            err = np.abs(c - ex)
+            res[label] = {"max_rel_err": float((err[big] / np.abs(ex[big])).max()),
+                          "max_err_over_sum_abs": float((err / ab).max())}
+        out[name] = res
+    return {"K": K, "M": M, "N": N, **out}
+
+
 CASES = {"act_quant_16384x7168": case_act, "wgrad_2048x7168x8192": case_wgrad,
-         "moe_grouped_256x(7168->2048)": case_moe}
-CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)"}
+         "moe_grouped_256x(7168->2048)": case_moe, "accum_precision_K4096": case_accum}
+CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)",
+             "accum": "accum_precision_K4096"}
 
 
 def oracle_fprop_sample(xb, wb, R, C):

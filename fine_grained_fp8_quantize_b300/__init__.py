@@ -23,7 +23,7 @@ __all__ = [
     "Fp8qError", "lib_path", "FP8Q_BF16", "FP8Q_FP32",
     "fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
     "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_workspace_size",
-    "fp8q_gemm_ws_static",
+    "fp8q_gemm_ws_static", "fp8q_gemm_unpromoted",
     "fp8q_grouped_gemm", "gemm_workspace",
     "fp8q_get_device_status", "fp8q_status_string", "fp8q_version",
     "quantize_act", "quantize_act_gather", "quantize_weight", "gemm", "grouped_gemm",
@@ -56,6 +56,7 @@ def _load():
     L.fp8q_gemm_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I32, P]
     L.fp8q_gemm_ws.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I32, P, ctypes.c_size_t, P]
     L.fp8q_gemm_ws_static.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I32, P]
+    L.fp8q_gemm_unpromoted.argtypes = [P, P, P, I64, I64, I64, P]
     L.fp8q_gemm_workspace_size.argtypes = []
     L.fp8q_gemm_workspace_size.restype = ctypes.c_size_t
     L.fp8q_grouped_gemm.argtypes = [P, P, P, P, P, P, ctypes.c_int32, I64, I64, I64, I32, P]
@@ -64,7 +65,7 @@ def _load():
     L.fp8q_status_string.argtypes = [I32]
     for name in ("fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
                  "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_ws_static",
-                 "fp8q_grouped_gemm",
+                 "fp8q_gemm_unpromoted", "fp8q_grouped_gemm",
                  "fp8q_get_device_status", "fp8q_version"):
         getattr(L, name).restype = I32
     return L
@@ -192,6 +193,17 @@ def fp8q_gemm_ws_static(Aq, sA, Bq, sB, C, sb_gran_n, stream=None):
     _check("fp8q_gemm_ws_static", _lib.fp8q_gemm_ws_static(
         _ptr(Aq), _ptr(sA), _ptr(Bq), _ptr(sB), _ptr(C), M, N, K, _out_dtype(C), int(sb_gran_n),
         _stream(stream)))
+
+
+def fp8q_gemm_unpromoted(Aq, Bq, C, stream=None):
+    """Diagnostic: C = Aq . Bq^T (decoded codes) accumulated over the whole K
+    inside the tensor core, without promotion or scales; C is FP32."""
+    _contig(Aq, Bq, C)
+    if C.dtype != torch.float32:
+        raise TypeError("fp8q_gemm_unpromoted writes FP32")
+    M, K = Aq.shape
+    N = Bq.shape[0]
+    _check("fp8q_gemm_unpromoted", _lib.fp8q_gemm_unpromoted(_ptr(Aq), _ptr(Bq), _ptr(C), M, N, K, _stream(stream)))
 
 
 def fp8q_grouped_gemm(Aq, sA, Bq, sB, C, row_offsets, stream=None):

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "fp8q.h"
+#include "diag.cuh"
 #include "gemm.cuh"
 #include "quantize.cuh"
 
@@ -144,13 +145,42 @@ int launch_quant_pipe(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   return launch_status();
 }
 
-// FP32 input, and BF16 rows + transposed columns in one pass (whose register
-// need allows 2 pipelined CTAs per SM, fewer than the 3 direct-load CTAs that
-// measure faster): one CTA per tile.  Other BF16 modes: the pipelined kernel.
+// BF16 row and/or transposed column groups: the split-role persistent kernel
+// (one 128-thread warpgroup per path), as many CTAs as fit on the device
+// (occupancy probed once per device).
+template <bool kRow, bool kCol>
+int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  DeviceInfo di;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  auto kern = quant_rc_kernel<kRow, kCol>;
+  constexpr int kSmem = rc_smem_bytes(kRow, kCol);
+  constexpr int kThreads = (kRow ? 128 : 0) + (kCol ? 128 : 0);
+  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmem) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  kern<<<grid, kThreads, kSmem, stream>>>(a, tiles);
+  return launch_status();
+}
+
+// FP32 input: one CTA per tile.  BF16 rows + transposed columns: the
+// split-role kernel (both paths busy).  Other BF16 modes (one path, or
+// 128x128 blocks): the pipelined kernel, which keeps 12 warps per SM where a
+// one-path split-role CTA would keep 8 (measured faster).
 template <int kMode>
 int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cudaStream_t s) {
   if (in_dtype == FP8Q_FP32) return launch_quant<true, kMode>(a, gx, gy, s);
-  if (kMode == (kQRow | kQCol)) return launch_quant<false, kMode>(a, gx, gy, s);
+  if constexpr (kMode == (kQRow | kQCol)) return launch_quant_rc<true, true>(a, gx * gy, s);
   return launch_quant_pipe<kMode>(a, gx * gy, s);
 }
 
@@ -471,6 +501,28 @@ int fp8q_gemm_ws_static(const uint8_t* Aq, const float* sA, const uint8_t* Bq, c
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(di.sms) * 4, cs) != cudaSuccess) return FP8Q_ERR_CUDA;
   return gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, sb_gran_n, nullptr, 0, cs, scratch, kStaticScratchBytes);
+}
+
+int fp8q_gemm_unpromoted(const uint8_t* Aq, const uint8_t* Bq, float* C, int64_t M, int64_t N, int64_t K,
+                         fp8q_stream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+    return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;
+  if (!Aq || !Bq || !C) return FP8Q_ERR_NULL;
+  if (!aligned16(Aq) || !aligned16(Bq) || !aligned16(C)) return FP8Q_ERR_ALIGN;
+  const int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, Aq, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kDiagBM)) return FP8Q_ERR_CUDA;
+  if (!make_tmap_u8(&tb, Bq, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kDiagBN)) return FP8Q_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_unpromoted_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kDiagSmem)) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>((M + kDiagBM - 1) / kDiagBM), static_cast<unsigned>((N + kDiagBN - 1) / kDiagBN));
+  if (grid.x > 2147483647u || grid.y > 65535u) return FP8Q_ERR_SHAPE;
+  gemm_unpromoted_kernel<<<grid, 128, kDiagSmem, reinterpret_cast<cudaStream_t>(stream)>>>(ta, tb, C, M, N, K);
+  return launch_status();
 }
 
 int fp8q_grouped_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const float* sB, void* C,

@@ -19,6 +19,8 @@
 // 16-byte transposed stores (a warp writes full 32-byte sectors).
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -353,6 +355,215 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
     // (bounded; the status word already records the timeout)
     for (uint32_t d = 0; d < 2; ++d) {
       const uint32_t u = it + d;  // iteration whose copy may be in flight
+      if (t + static_cast<int64_t>(d) * gridDim.x >= num_tiles) break;
+      const uint64_t s0 = globaltimer_ns();
+      while (!mbar_try_wait(bar0 + 8 * (u & 1u), (u >> 1) & 1u) && globaltimer_ns() - s0 < 1000000ull) {}
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rows + transposed columns of BF16 activations in one pass, split by role.
+// Persistent, 256 threads, two 128 x 128 tiles in flight per CTA (bulk
+// copies, one 256-byte row per copy, into rows of a padded 272-byte pitch).
+//   warps 0-3  row path: thread r owns tile row r (16 x 16-byte reads); its
+//              1x128 amax is a packed BF16 max over the row (no shuffles).
+//   warps 4-7  column path: thread (p, h) owns columns 2p, 2p+1 over the
+//              64 rows of half h (64 x 4-byte reads); the two halves meet in
+//              shared memory for the 128x1 amax.
+// Each path writes its 128 x 128 codes into a staged shared-memory tile and
+// then copies it out with whole 128-byte lines per 8 lanes, so every global
+// store instruction writes full sectors.  The padded pitches keep the
+// shared-memory reads and writes near conflict-free.  The amax is exact in
+// BF16; the scale and cast are those of quant_tile_body.
+// ---------------------------------------------------------------------------
+constexpr int kRcPitch = 272;                 // bytes per smem tile row
+constexpr int kRcTileBytes = 128 * kRcPitch;  // one tile buffer
+constexpr int kRcCodePitch = 144;             // bytes per row of a staged 128 x 128 code tile
+constexpr int kRcCodeBytes = 128 * kRcCodePitch;
+constexpr int kRcSmem = 2 * kRcTileBytes + 2 * kRcCodeBytes;  // inputs, row codes, transposed codes
+
+__device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
+__device__ __forceinline__ uint32_t u32_of(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// Shared memory of quant_rc_kernel<kRow, kCol>: two input tiles, then one
+// staged code tile per path.
+constexpr int rc_smem_bytes(bool row, bool col) {
+  return 2 * kRcTileBytes + ((row ? 1 : 0) + (col ? 1 : 0)) * kRcCodeBytes;
+}
+
+template <bool kRow, bool kCol>
+__global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
+    quant_rc_kernel(const QuantArgs args, int64_t num_tiles) {
+  extern __shared__ __align__(128) uint8_t rsm[];  // [2][128][kRcPitch] inputs, then the staged code tiles
+  __shared__ float s_cmax[2][128];                 // column maxima of each 64-row half
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+
+  const int tid = threadIdx.x;
+  const int64_t K = args.K;
+  const int64_t M = args.M;
+  const int64_t kbt = K >> 7;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  const uint32_t buf0 = smem_u32(rsm);
+
+  // bytes that land for tile tt (rows past M are not copied)
+  // (with column groups every tile is full and rows are not gathered)
+  auto tile_bytes = [&](int64_t tt) -> uint32_t {
+    if constexpr (kCol) return 128u * 256u;
+    const int64_t rows = M - (tt / kbt) * 128;
+    return static_cast<uint32_t>(rows < 128 ? rows : 128) * 256u;
+  };
+  auto issue_row = [&](int64_t tt, int b) {  // threads 0..127: tile row tid, through the row gather
+    const int64_t m = (tt / kbt) * 128 + tid;
+    if constexpr (kCol) {
+      bulk_load(buf0 + b * kRcTileBytes + tid * kRcPitch,
+                static_cast<const uint16_t*>(args.x) + m * K + (tt % kbt) * 128, 256u, bar0 + 8 * b);
+    } else if (m < M) {
+      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
+      bulk_load(buf0 + b * kRcTileBytes + tid * kRcPitch,
+                static_cast<const uint16_t*>(args.x) + src * K + (tt % kbt) * 128, 256u, bar0 + 8 * b);
+    }
+  };
+  // the row path runs on threads 0..127; the column path on the next 128
+  // (or on 0..127 when it is alone)
+  const bool row_role = kRow && (!kCol || tid < 128);
+  const int ctid = kRow ? tid - 128 : tid;
+
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t t0 = blockIdx.x, t1 = blockIdx.x + gridDim.x;
+  if (tid == 0) {
+    if (t0 < num_tiles) mbar_arrive_expect_tx(bar0, tile_bytes(t0));
+    if (t1 < num_tiles) mbar_arrive_expect_tx(bar0 + 8, tile_bytes(t1));
+  }
+  __syncthreads();
+  if (tid < 128) {
+    if (t0 < num_tiles) issue_row(t0, 0);
+    if (t1 < num_tiles) issue_row(t1, 1);
+  }
+
+  uint32_t it = 0;
+  int64_t t = t0;
+  for (; t < num_tiles; t += gridDim.x, ++it) {
+    const int b = it & 1;
+    const bool ok = mbar_wait(bar0 + 8 * b, (it >> 1) & 1u, abort_flag);
+    const uint8_t* tile = rsm + b * kRcTileBytes;
+    const int64_t kb = t % kbt, mb = t / kbt;
+    const int64_t k0 = kb * 128, m0 = mb * 128;
+    // one register array for either path (the paths are warp-uniform, so
+    // only one of them is ever live): row path, the row's 128 values as 16
+    // x 4 words; column path, columns 2p, 2p+1 of 64 rows, one word each
+    uint32_t w[64];
+    const int p = ctid & 63;
+    const int hh = ctid >> 6;
+    if (ok) {
+      if (row_role) {
+        const uint4* rp = reinterpret_cast<const uint4*>(tile + tid * kRcPitch);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 q = rp[i];
+          w[4 * i] = q.x;
+          w[4 * i + 1] = q.y;
+          w[4 * i + 2] = q.z;
+          w[4 * i + 3] = q.w;
+        }
+      } else {
+        const uint8_t* cp = tile + (hh * 64) * kRcPitch + p * 4;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) w[r] = *reinterpret_cast<const uint32_t*>(cp + r * kRcPitch);
+      }
+    }
+    const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
+    if (ok && tid == 0 && tn < num_tiles) mbar_arrive_expect_tx(bar0 + 8 * b, tile_bytes(tn));
+    // every thread has its values (buffer b is free) or some wait failed
+    if (__syncthreads_or(!ok)) break;
+    if (tid < 128 && tn < num_tiles) issue_row(tn, b);
+
+    if (row_role) {
+      // ---- 1x128 row group of row m
+      const int64_t m = m0 + tid;
+      __nv_bfloat162 mx = __habs2(bf2_of(w[0]));
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = __hmax2(mx, __habs2(bf2_of(w[i])));
+      const uint32_t mw = u32_of(mx);
+      float sc, inv;
+      group_scale(fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), sc, inv);
+      if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
+      uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        uint32_t c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t a = w[4 * i + 2 * u], bb = w[4 * i + 2 * u + 1];
+          c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
+                            bf16hi_to_f32(bb) * inv);
+        }
+        st[i >> 1] = make_uint4(c[0], c[1], c[2], c[3]);
+      }
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+      // copy out: 8 lanes per 128-byte row, 4 rows per instruction
+      const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = warp * 32 + j * 4 + (lane >> 3);
+        const int64_t mr = m0 + r;
+        const uint4 q = *reinterpret_cast<const uint4*>(rsm + 2 * kRcTileBytes + r * kRcCodePitch + (lane & 7) * 16);
+        if (mr < M) *reinterpret_cast<uint4*>(args.q_row + mr * K + k0 + (lane & 7) * 16) = q;
+      }
+    } else if constexpr (kCol) {
+      // ---- 128x1 column groups of columns k0 + 2p, k0 + 2p + 1
+      __nv_bfloat162 mx = __habs2(bf2_of(w[0]));
+#pragma unroll
+      for (int r = 1; r < 64; ++r) mx = __hmax2(mx, __habs2(bf2_of(w[r])));
+      const uint32_t mw = u32_of(mx);
+      s_cmax[hh][2 * p] = bf16lo_to_f32(mw);
+      s_cmax[hh][2 * p + 1] = bf16hi_to_f32(mw);
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      float sc0, inv0, sc1, inv1;
+      group_scale(fmaxf(s_cmax[0][2 * p], s_cmax[1][2 * p]), sc0, inv0);
+      group_scale(fmaxf(s_cmax[0][2 * p + 1], s_cmax[1][2 * p + 1]), sc1, inv1);
+      if (hh == 0) *reinterpret_cast<float2*>(args.s_col + mb * K + k0 + 2 * p) = make_float2(sc0, sc1);
+      // staged transposed tile: row = column of x, 128 token bytes per row
+      uint8_t* ct = rsm + 2 * kRcTileBytes + (kRow ? kRcCodeBytes : 0);
+      uint4* d0 = reinterpret_cast<uint4*>(ct + (2 * p) * kRcCodePitch + hh * 64);
+      uint4* d1 = reinterpret_cast<uint4*>(ct + (2 * p + 1) * kRcCodePitch + hh * 64);
+#pragma unroll
+      for (int r = 0; r < 64; r += 16) {
+        uint32_t c0[4], c1[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t a = w[r + 4 * u], bb = w[r + 4 * u + 1], cc = w[r + 4 * u + 2], dd = w[r + 4 * u + 3];
+          c0[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv0, bf16lo_to_f32(bb) * inv0, bf16lo_to_f32(cc) * inv0,
+                             bf16lo_to_f32(dd) * inv0);
+          c1[u] = cvt_e4m3x4(bf16hi_to_f32(a) * inv1, bf16hi_to_f32(bb) * inv1, bf16hi_to_f32(cc) * inv1,
+                             bf16hi_to_f32(dd) * inv1);
+        }
+        d0[r >> 4] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+        d1[r >> 4] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+      }
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      // copy out: 8 lanes per 128-byte row of the transposed output
+      const int cw = ctid >> 5, lane = tid & 31;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = cw * 32 + j * 4 + (lane >> 3);
+        const uint4 q = *reinterpret_cast<const uint4*>(ct + r * kRcCodePitch + (lane & 7) * 16);
+        *reinterpret_cast<uint4*>(args.q_colT + (k0 + r) * M + m0 + (lane & 7) * 16) = q;
+      }
+    }
+  }
+  if (t < num_tiles) {
+    // a wait failed: let every copy this CTA issued land before it exits
+    for (uint32_t d = 0; d < 2; ++d) {
+      const uint32_t u = it + d;
       if (t + static_cast<int64_t>(d) * gridDim.x >= num_tiles) break;
       const uint64_t s0 = globaltimer_ns();
       while (!mbar_try_wait(bar0 + 8 * (u & 1u), (u >> 1) & 1u) && globaltimer_ns() - s0 < 1000000ull) {}

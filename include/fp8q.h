@@ -259,6 +259,20 @@ FP8Q_API int fp8q_grouped_gemm(const uint8_t *Aq, const float *sA, const uint8_t
                       int64_t N, int64_t K, int out_dtype, fp8q_stream_t stream);
 
 /*
+ * fp8q_gemm_unpromoted -- accumulation-precision diagnostic, not part of the
+ * method: C = Aq . Bq^T over the decoded E4M3 codes with the WHOLE K
+ * accumulated inside the tensor core (no promotion to FP32 registers, no
+ * scales), FP32 out.  The pages report that limited tensor-core accumulation
+ * precision reaches a maximum relative error near 2% for an inner dimension
+ * of 4096 ("Eliminate Deepseek Ai News For Good", the accumulation-precision
+ * sentence); comparing this against fp8q_gemm with unit scales measures that
+ * effect on B300.  Aq [M][K], Bq [N][K] (K contiguous), C [M][N] FP32.
+ * M >= 0, N % 128 == 0, K % 128 == 0.  Unoptimized (one tile per CTA).
+ */
+FP8Q_API int fp8q_gemm_unpromoted(const uint8_t *Aq, const uint8_t *Bq, float *C,
+                         int64_t M, int64_t N, int64_t K, fp8q_stream_t stream);
+
+/*
  * fp8q_get_device_status -- synchronizes `stream`, then returns and clears
  * the current device's status word: FP8Q_OK, or FP8Q_ERR_TIMEOUT if a
  * kernel's bounded pipeline wait expired since the last call, or
