@@ -373,7 +373,7 @@ def case_act(args, f, torch, synth, pk, iters):
     check_status(f, "after the activation quantization")
     nbytes = T * H * 2 + 2 * T * H + 2 * (T * H // 128) * 4
     return {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes,
-            "roofline": hbm_roofline("quant_tile_kernel<bf16, row|col>", nbytes, ms, pk, "act_16384x7168")}
+            "roofline": hbm_roofline("quant_rc_kernel<bf16, row|col>", nbytes, ms, pk, "act_16384x7168")}
 
 
 def case_wgrad(args, f, torch, synth, pk, iters):
