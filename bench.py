@@ -496,23 +496,29 @@ def oracle_fprop_sample(xb, wb, R, C):
     return time.perf_counter() - t, 2.0 * R * C * K
 
 
+def _scale_sample(R, C, factor):
+    """Scale the sample's work (R x C outputs) by `factor`: R rows first,
+    then C columns (a multiple of 128) once R holds every row."""
+    M, N = FPROP["M"], FPROP["N"]
+    R2 = int(min(M, max(1, R * factor)))
+    C2 = int(min(N, max(128, round(R * C * factor / R2 / 128) * 128)))
+    return R2, C2
+
+
 def oracle_sample_size(xb, wb, seconds):
     """(R, C) whose oracle_fprop_sample takes about `seconds`: R rows of X and
     C (a multiple of 128) output columns.  The GEMM dominates the fprop step
-    at full size, so the sample keeps C small (weight quantization is a small
-    share) and grows R first; two calibration runs fit
-    t(R, 128) = fixed + R * per_row."""
+    at full size, so the sample grows R first and keeps C small (weight
+    quantization is a small share).  Calibration runs grow the sample until
+    one takes a quarter of the budget; the time of that run sets the size."""
     M, N = FPROP["M"], FPROP["N"]
-    r1, r2 = 32, 128
-    t1, _ = oracle_fprop_sample(xb, wb, r1, 128)
-    t2, _ = oracle_fprop_sample(xb, wb, r2, 128)
-    per_row = max((t2 - t1) / (r2 - r1), 1e-7)
-    fixed = max(t1 - r1 * per_row, 0.0)
-    R = int(min(M, max(1, (seconds - fixed) / per_row)))
-    C = 128
-    if R == M:
-        C = int(min(N, max(128, 128 * (seconds // (fixed + M * per_row)))))
-    return R, C
+    R, C = 128, 128
+    while True:
+        dt, _ = oracle_fprop_sample(xb, wb, R, C)
+        if dt >= seconds / 4 or (R == M and C == N):
+            break
+        R, C = _scale_sample(R, C, min(8.0, seconds / 2 / max(dt, 1e-3)))
+    return _scale_sample(R, C, seconds / max(dt, 1e-6))
 
 
 def cpu_baseline_fprop(X, W, budget_s):
