@@ -11,7 +11,9 @@ Functions take and return numpy arrays on the host:
     ``float32``;
   * E4M3 codes are ``uint8``; scales are ``float32``;
   * scale layouts are K-block-major: ``s_row[K/128][M]``, ``s_col[M/128][K]``,
-    weight ``s[N/128][K/128]``, Wgrad per-column ``sB[K/128][N]``.
+    weight ``s[N/128][K/128]``, Wgrad per-column ``sB[K/128][N]``;
+  * the MX variant's scales are E8M0 bytes (``uint8``), row-major
+    ``e8[rows][K/32]``.
 """
 import ctypes
 import os
@@ -50,6 +52,10 @@ def lib():
         L.oracle_grouped_gemm_points.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                                  P, P, I64, P, P, P]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_mx_shared_exp.restype = ctypes.c_int
+        L.oracle_mx_shared_exp.argtypes = [ctypes.c_float]
+        L.oracle_mx_quantize_rows.argtypes = [P, I32, I64, I64, P, P]
+        L.oracle_mx_gemm_points.argtypes = [P, P, P, P, I64, P, P, I64, P, P]
         _lib = L
     return _lib
 
@@ -187,3 +193,34 @@ def grouped_gemm_points(Aq, sA, Bq, sB, row_offsets, m_idx, n_idx):
     lib().oracle_grouped_gemm_points(_ptr(Aq), _ptr(sA), _ptr(Bq), _ptr(sB), _ptr(off), E, T,
                                      N, K, _ptr(mi), _ptr(ni), n, _ptr(ex), _ptr(ab), _ptr(pg))
     return ex, ab, pg
+
+
+def mx_shared_exp(amax):
+    """Shared exponent of an MX group whose largest magnitude is ``amax``."""
+    return lib().oracle_mx_shared_exp(ctypes.c_float(amax))
+
+
+def mx_quantize_rows(x):
+    """MX 1x32 groups: x[M,K] -> (q[M,K] u8 E4M3 codes, e8[M,K/32] u8 E8M0 bytes)."""
+    x, dt = _xin(x)
+    M, K = x.shape
+    assert K % 32 == 0
+    q = np.empty((M, K), np.uint8)
+    e8 = np.empty((M, K // 32), np.uint8)
+    lib().oracle_mx_quantize_rows(_ptr(x), dt, M, K, _ptr(q), _ptr(e8))
+    return q, e8
+
+
+def mx_gemm_points(Aq, ea, Bq, eb, m_idx, n_idx):
+    """MX GEMM at points -> (C_exact f64, absref f64), each [npts]."""
+    Aq = _c(Aq, np.uint8); Bq = _c(Bq, np.uint8)
+    ea = _c(ea, np.uint8); eb = _c(eb, np.uint8)
+    mi = _c(m_idx, np.int64); ni = _c(n_idx, np.int64)
+    K = Aq.shape[1]
+    assert Bq.shape[1] == K and ea.shape == (Aq.shape[0], K // 32) and eb.shape == (Bq.shape[0], K // 32)
+    n = mi.size
+    ex = np.empty(n, np.float64)
+    ab = np.empty(n, np.float64)
+    lib().oracle_mx_gemm_points(_ptr(Aq), _ptr(ea), _ptr(Bq), _ptr(eb), K, _ptr(mi), _ptr(ni), n,
+                                _ptr(ex), _ptr(ab))
+    return ex, ab

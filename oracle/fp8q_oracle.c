@@ -391,6 +391,116 @@ void oracle_grouped_gemm_points(const uint8_t *Aq, const float *sA,
     }
 }
 
+/* ------------------------------------------------------------------ */
+/* MX variant: 1x32 groups with power-of-two (E8M0) scales             */
+/* ------------------------------------------------------------------ */
+/*
+ * Source: "Deepseek Ai News Expert Interview" (page 2), the DualPipe /
+ * microscaling paragraph: the fine-grained strategy follows the microscaling
+ * (MX) formats of Rouhani et al. (2023), and Blackwell tensor cores support
+ * those formats with smaller groups.  The pages give no MX algorithm, so this
+ * is the conversion the MX formats themselves define, in its plainest form:
+ *  - a group is 32 consecutive elements along K of one row;
+ *  - its shared exponent is floor(log2(amax)) minus 8, the exponent of the
+ *    largest normal E4M3 binade (448 = 1.75 * 2^8), clamped to E8M0's
+ *    [-127, 127]; a group whose amax is 0 takes -127;
+ *  - the scale is X = 2^shared_exp, stored as the E8M0 byte shared_exp + 127;
+ *  - each element is E4M3(fl32(x / X)) with the RNE satfinite cast above.
+ *    x / X reaches up to 511.x, so the group's largest elements can
+ *    saturate to 448.
+ * Dequantization: x ~ decode(q) * 2^(byte - 127).  Dividing by a power of two
+ * is exact in fl32 except below FP32's subnormal range, where the E4M3 cast
+ * gives zero anyway.
+ */
+#define MX_GROUP 32
+#define E4M3_EMAX 8
+
+int oracle_mx_shared_exp(float amax)
+{
+    int e, se;
+    if (!(amax > 0.0f))
+        return -127;
+    (void)frexpf(amax, &e);            /* amax = f * 2^e, f in [0.5, 1) */
+    se = (e - 1) - E4M3_EMAX;          /* floor(log2(amax)) - 8 */
+    if (se < -127)
+        se = -127;
+    if (se > 127)
+        se = 127;
+    return se;
+}
+
+/* x[M][K] row-major -> q[M][K] codes, e8[M][K/32] E8M0 scale bytes
+   (plain row-major here; the GPU's tiled layout is a permutation of it). */
+void oracle_mx_quantize_rows(const void *x, int dtype, int64_t M, int64_t K,
+                             uint8_t *q, uint8_t *e8)
+{
+    int64_t G = K / MX_GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t g = 0; g < G; ++g) {
+            float amax = 0.0f;
+            for (int64_t j = 0; j < MX_GROUP; ++j) {
+                float v = fabsf(load_x(x, dtype, m * K + g * MX_GROUP + j));
+                if (v > amax)
+                    amax = v;
+            }
+            int se = oracle_mx_shared_exp(amax);
+            float X = ldexpf(1.0f, se);
+            e8[m * G + g] = (uint8_t)(se + 127);
+            for (int64_t j = 0; j < MX_GROUP; ++j) {
+                int64_t i = m * K + g * MX_GROUP + j;
+                volatile float v = load_x(x, dtype, i) / X;   /* fl32(x / X) */
+                q[i] = oracle_e4m3_encode(v);
+            }
+        }
+    }
+}
+
+/* One output of the MX GEMM,
+ *   C[m][n] = sum_g 2^(ea[m][g] - 127) * 2^(eb[n][g] - 127) * P_g,
+ *   P_g = sum_{k in group g} decode(Aq[m][k]) * decode(Bq[n][k]).
+ * Each P_g is exact in fp64 (32 products of 4-bit significands); the groups
+ * are summed in fp64.  absref = sum_k |a_dq * b_dq|. */
+static void mx_gemm_one(const uint8_t *Aq, const uint8_t *ea, const uint8_t *Bq,
+                        const uint8_t *eb, int64_t K, int64_t m, int64_t n,
+                        double *exact, double *absref)
+{
+    int64_t G = K / MX_GROUP;
+    double ex = 0.0, ab = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+        double p = 0.0, pabs = 0.0;
+        for (int64_t j = 0; j < MX_GROUP; ++j) {
+            int64_t k = g * MX_GROUP + j;
+            double prod = g_decode[Aq[m * K + k]] * g_decode[Bq[n * K + k]];
+            p += prod;
+            pabs += fabs(prod);
+        }
+        double scale = ldexp(1.0, (int)ea[m * G + g] - 127 + (int)eb[n * G + g] - 127);
+        ex += scale * p;
+        ab += scale * pabs;
+    }
+    *exact = ex;
+    *absref = ab;
+}
+
+/* MX GEMM at listed points (m_idx[i], n_idx[i]).  Aq[M][K], ea[M][K/32],
+   Bq[N][K], eb[N][K/32]. */
+void oracle_mx_gemm_points(const uint8_t *Aq, const uint8_t *ea, const uint8_t *Bq,
+                           const uint8_t *eb, int64_t K, const int64_t *m_idx,
+                           const int64_t *n_idx, int64_t npts, double *c_exact,
+                           double *c_absref)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < npts; ++i) {
+        double ex, ab;
+        mx_gemm_one(Aq, ea, Bq, eb, K, m_idx[i], n_idx[i], &ex, &ab);
+        if (c_exact)
+            c_exact[i] = ex;
+        if (c_absref)
+            c_absref[i] = ab;
+    }
+}
+
 /* Number of OpenMP threads the oracle runs on (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -10,7 +10,8 @@ import pytest
 from conftest import ROOT
 
 SRC = os.path.join(ROOT, "oracle", "fp8q_oracle.c")
-PINS = ["tests/test_oracle_codec.py", "tests/test_oracle_quant.py", "tests/test_oracle_gemm.py"]
+PINS = ["tests/test_oracle_codec.py", "tests/test_oracle_quant.py", "tests/test_oracle_gemm.py",
+        "tests/test_oracle_mx.py"]
 
 MUTATIONS = {
     "ties_away_from_zero": ("r = nearbyint(a / quantum) * quantum;",
@@ -24,6 +25,13 @@ MUTATIONS = {
     "gemm_B_transposed": ("g_decode[Bq[n * K + k]]", "g_decode[Bq[k * N + n]]"),
     "gemm_sA_index": ("float sa = sA[kb * lds_a + m];", "float sa = sA[m * KB + kb];"),
     "gemm_pages_order_drops_scale": ("volatile float t = pf * s;", "volatile float t = pf;"),
+    "mx_ceil_exponent": ("se = (e - 1) - E4M3_EMAX;", "se = e - E4M3_EMAX;"),
+    "mx_no_lower_clamp": ("    if (se < -127)\n        se = -127;\n", ""),
+    "mx_multiplies_by_scale": ("load_x(x, dtype, i) / X;", "load_x(x, dtype, i) * X;"),
+    "mx_group_of_16_in_amax": ("for (int64_t j = 0; j < MX_GROUP; ++j) {\n                float v = fabsf(",
+                               "for (int64_t j = 0; j < MX_GROUP / 2; ++j) {\n                float v = fabsf("),
+    "mx_gemm_drops_eb": ("(int)ea[m * G + g] - 127 + (int)eb[n * G + g] - 127", "(int)ea[m * G + g] - 127"),
+    "mx_gemm_b_scale_index": ("(int)eb[n * G + g]", "(int)eb[g * G + n]"),
 }
 
 
