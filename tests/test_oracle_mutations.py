@@ -22,7 +22,8 @@ MUTATIONS = {
                              "float v = fabsf(load_x(x, dtype, k * M + mb * GROUP + j));"),
     "weight_scale_index_swapped": ("s_blk[nb * KB + kb] = s;", "s_blk[kb * NB + nb] = s;"),
     "gemm_dropped_sB": ("ex += ((double)sa * (double)sb) * p;", "ex += (double)sa * p;"),
-    "gemm_B_transposed": ("g_decode[Bq[n * K + k]]", "g_decode[Bq[k * N + n]]"),
+    "gemm_B_transposed": ("int64_t k = kb * GROUP + j;\n            double prod = g_decode[Aq[m * K + k]] * g_decode[Bq[n * K + k]];",
+                          "int64_t k = kb * GROUP + j;\n            double prod = g_decode[Aq[m * K + k]] * g_decode[Bq[k * N + n]];"),
     "gemm_sA_index": ("float sa = sA[kb * lds_a + m];", "float sa = sA[m * KB + kb];"),
     "gemm_pages_order_drops_scale": ("volatile float t = pf * s;", "volatile float t = pf;"),
     "mx_ceil_exponent": ("se = (e - 1) - E4M3_EMAX;", "se = e - E4M3_EMAX;"),
