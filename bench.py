@@ -55,7 +55,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
-    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum"],
+    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum", "mx"],
                    help="all: the Fprop step plus the breakdown; else time one workload alone")
     p.add_argument("--no-breakdown", action="store_true", help="time the Fprop step only")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
@@ -475,10 +475,45 @@ def case_accum(args, f, torch, synth, pk, iters):
     return {"K": K, "M": M, "N": N, **out}
 
 
+def case_mx(args, f, torch, synth, pk, iters):
+    """MX variant of the Fprop step 4096x18432x7168: 1x32 groups with E8M0
+    scales (X and W), GEMM with the scales applied by the tensor core; and the
+    MX quantizer alone on the 16384x7168 activation."""
+    X, W = synth.fprop_inputs(device="cuda")
+    M, K = X.shape
+    N = W.shape[0]
+    qx = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    sx = torch.empty(f.fp8q_mx_scale_bytes(M, K), dtype=torch.uint8, device="cuda")
+    qw = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    sw = torch.empty(f.fp8q_mx_scale_bytes(N, K), dtype=torch.uint8, device="cuda")
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    f.fp8q_mx_quantize(X, qx, sx)
+    f.fp8q_mx_quantize(W, qw, sw)
+    ms_g = _time(torch, lambda: f.fp8q_mx_gemm(qx, sx, qw, sw, C), iters)
+    ms_all = _time(torch, lambda: (f.fp8q_mx_quantize(X, qx, sx), f.fp8q_mx_quantize(W, qw, sw),
+                                   f.fp8q_mx_gemm(qx, sx, qw, sw, C)), iters)
+    del X, W, qx, sx, qw, sw, C
+    T, H = ACT["T"], ACT["H"]
+    Xa = synth.act_quant_inputs(device="cuda")
+    qa = torch.empty(T, H, dtype=torch.uint8, device="cuda")
+    sa = torch.empty(f.fp8q_mx_scale_bytes(T, H), dtype=torch.uint8, device="cuda")
+    ms_q = _time(torch, lambda: f.fp8q_mx_quantize(Xa, qa, sa), iters)
+    check_status(f, "after the MX variant")
+    fl = 2.0 * M * N * K
+    qbytes = T * H * 2 + T * H + f.fp8q_mx_scale_bytes(T, H)
+    return {"gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
+            "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
+            "roofline": tensor_roofline("gemm_mx_kernel<bf16 out>", fl, ms_g, pk, "mx_fprop_4096x18432x7168"),
+            "act_quant_16384x7168": {
+                "ms": round(ms_q, 4), "GB/s": round(qbytes / (ms_q * 1e-3) / 1e9, 1), "bytes": qbytes,
+                "roofline": hbm_roofline("quant_mx_kernel<bf16>", qbytes, ms_q, pk, "mx_act_16384x7168")}}
+
+
 CASES = {"act_quant_16384x7168": case_act, "wgrad_2048x7168x8192": case_wgrad,
-         "moe_grouped_256x(7168->2048)": case_moe, "accum_precision_K4096": case_accum}
+         "moe_grouped_256x(7168->2048)": case_moe, "accum_precision_K4096": case_accum,
+         "mx_fprop_4096x18432x7168": case_mx}
 CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)",
-             "accum": "accum_precision_K4096"}
+             "accum": "accum_precision_K4096", "mx": "mx_fprop_4096x18432x7168"}
 
 
 def oracle_fprop_sample(xb, wb, R, C):

@@ -60,12 +60,16 @@ def _load():
     L.fp8q_gemm_workspace_size.argtypes = []
     L.fp8q_gemm_workspace_size.restype = ctypes.c_size_t
     L.fp8q_grouped_gemm.argtypes = [P, P, P, P, P, P, ctypes.c_int32, I64, I64, I64, I32, P]
+    L.fp8q_mx_scale_bytes.argtypes = [I64, I64]
+    L.fp8q_mx_scale_bytes.restype = ctypes.c_size_t
+    L.fp8q_mx_quantize.argtypes = [P, I32, I64, I64, P, P, P]
+    L.fp8q_mx_gemm.argtypes = [P, P, P, P, P, I64, I64, I64, I32, P]
     L.fp8q_get_device_status.argtypes = [P]
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [I32]
     for name in ("fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
                  "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_ws_static",
-                 "fp8q_gemm_unpromoted", "fp8q_grouped_gemm",
+                 "fp8q_gemm_unpromoted", "fp8q_grouped_gemm", "fp8q_mx_quantize", "fp8q_mx_gemm",
                  "fp8q_get_device_status", "fp8q_version"):
         getattr(L, name).restype = I32
     return L
@@ -217,6 +221,30 @@ def fp8q_grouped_gemm(Aq, sA, Bq, sB, C, row_offsets, stream=None):
         _out_dtype(C), _stream(stream)))
 
 
+def fp8q_mx_scale_bytes(rows, K):
+    return _lib.fp8q_mx_scale_bytes(rows, K)
+
+
+def fp8q_mx_quantize(x, q, s, stream=None):
+    """MX 1x32 quantization: x[rows,K] -> q[rows,K] codes, s tiled E8M0 scales (uint8)."""
+    _contig(x, q, s)
+    rows, K = x.shape
+    if s is not None and s.numel() < fp8q_mx_scale_bytes(rows, K):
+        raise ValueError("scale buffer smaller than fp8q_mx_scale_bytes(rows, K)")
+    _check("fp8q_mx_quantize", _lib.fp8q_mx_quantize(_ptr(x), _in_dtype(x), rows, K, _ptr(q), _ptr(s),
+                                                     _stream(stream)))
+
+
+def fp8q_mx_gemm(Aq, sA, Bq, sB, C, stream=None):
+    _contig(Aq, sA, Bq, sB, C)
+    M, K = Aq.shape
+    N = Bq.shape[0]
+    if sA.numel() < fp8q_mx_scale_bytes(M, K) or sB.numel() < fp8q_mx_scale_bytes(N, K):
+        raise ValueError("scale buffer smaller than fp8q_mx_scale_bytes")
+    _check("fp8q_mx_gemm", _lib.fp8q_mx_gemm(_ptr(Aq), _ptr(sA), _ptr(Bq), _ptr(sB), _ptr(C), M, N, K,
+                                             _out_dtype(C), _stream(stream)))
+
+
 def fp8q_get_device_status(stream=None):
     return _lib.fp8q_get_device_status(_stream(stream))
 
@@ -285,4 +313,19 @@ def gemm(Aq, sA, Bq, sB, out_dtype=torch.bfloat16, sb_gran_n=128, workspace=None
 def grouped_gemm(Aq, sA, Bq, sB, row_offsets, out_dtype=torch.bfloat16, stream=None):
     C = torch.empty(Aq.shape[0], Bq.shape[1], dtype=out_dtype, device=Aq.device)
     fp8q_grouped_gemm(Aq, sA, Bq, sB, C, row_offsets, stream)
+    return C
+
+
+def mx_quantize(x, stream=None):
+    """MX variant: -> (q [rows, K] uint8 codes, s tiled E8M0 scales, uint8)."""
+    rows, K = x.shape
+    q = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    s = torch.empty(fp8q_mx_scale_bytes(rows, K), dtype=torch.uint8, device=x.device)
+    fp8q_mx_quantize(x, q, s, stream)
+    return q, s
+
+
+def mx_gemm(Aq, sA, Bq, sB, out_dtype=torch.bfloat16, stream=None):
+    C = torch.empty(Aq.shape[0], Bq.shape[0], dtype=out_dtype, device=Aq.device)
+    fp8q_mx_gemm(Aq, sA, Bq, sB, C, stream)
     return C

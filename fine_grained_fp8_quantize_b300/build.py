@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfp8q.so")
 SOURCES = [os.path.join(CSRC, "fp8q.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quantize.cuh", "gemm.cuh", "diag.cuh")] + \
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quantize.cuh", "gemm.cuh", "diag.cuh", "mx.cuh")] + \
     [os.path.join(INCLUDE, "fp8q.h")]
 
 NVCC_FLAGS = [

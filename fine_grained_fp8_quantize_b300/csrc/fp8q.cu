@@ -1,7 +1,7 @@
 // fp8q.cu -- libfp8q.so: the C ABI declared in include/fp8q.h.
 //
 // Host side only validates arguments, builds TMA tensor maps and launches
-// the kernels of quantize.cuh / gemm.cuh on the caller's stream.  It never
+// the kernels of quantize.cuh / gemm.cuh / mx.cuh on the caller's stream.  It never
 // allocates device memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -14,6 +14,7 @@
 #include "fp8q.h"
 #include "diag.cuh"
 #include "gemm.cuh"
+#include "mx.cuh"
 #include "quantize.cuh"
 
 namespace {
@@ -316,6 +317,71 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
              : launch_gemm_t<false, 128, false>(ta, tb, tc, a, grid, stream);
 }
 
+// MX variant: bytes of the tiled E8M0 scale array of a rows x K operand.
+size_t mx_scale_bytes(int64_t rows, int64_t K) {
+  return static_cast<size_t>(K / 128) * static_cast<size_t>((rows + 127) / 128) * 512u;
+}
+
+template <bool kF32>
+int launch_quant_mx(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  DeviceInfo di;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  auto kern = quant_mx_kernel<kF32>;
+  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMxQuantThreads, 0) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t tiles = (K / 128) * ((rows + 127) / 128);
+  const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
+  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+  kern<<<grid, kMxQuantThreads, 0, stream>>>(x, rows, K, q, s, tiles);
+  return launch_status();
+}
+
+int mx_gemm_common(const uint8_t* Aq, const uint8_t* sA, const uint8_t* Bq, const uint8_t* sB, void* C, int64_t M,
+                   int64_t N, int64_t K, int out_dtype, cudaStream_t stream) {
+  if (out_dtype != FP8Q_BF16 && out_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+    return FP8Q_ERR_SHAPE;
+  const int64_t tiles_m = (M + kMxBM - 1) / kMxBM, tiles_n = (N + kMxBN - 1) / kMxBN;
+  if (tiles_m * tiles_n > (int64_t(1) << 31) - 1) return FP8Q_ERR_SHAPE;
+  if (M == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!Aq || !sA || !Bq || !sB || !C) return FP8Q_ERR_NULL;
+  if (!aligned16(Aq) || !aligned16(sA) || !aligned16(Bq) || !aligned16(sB) || !aligned16(C)) return FP8Q_ERR_ALIGN;
+  DeviceInfo di;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  CUtensorMap ta, tb, tc;
+  if (!make_tmap_u8(&ta, Aq, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kMxBM)) return FP8Q_ERR_CUDA;
+  if (!make_tmap_u8(&tb, Bq, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kMxBN)) return FP8Q_ERR_CUDA;
+  if (!make_tmap_out(&tc, C, out_dtype == FP8Q_FP32, static_cast<uint64_t>(N), static_cast<uint64_t>(M)))
+    return FP8Q_ERR_CUDA;
+  MxGemmArgs a;
+  a.sA = sA;
+  a.sB = sB;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.tiles_m = static_cast<int>(tiles_m);
+  a.tiles_n = static_cast<int>(tiles_n);
+  const int64_t tiles = tiles_m * tiles_n;
+  const int grid = static_cast<int>(tiles < di.sms ? tiles : di.sms);
+  auto kern = out_dtype == FP8Q_FP32 ? gemm_mx_kernel<true> : gemm_mx_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMxSmem)) !=
+      cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  kern<<<grid, kMxThreads, kMxSmem, stream>>>(ta, tb, tc, a);
+  return launch_status();
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -532,6 +598,28 @@ int fp8q_grouped_gemm(const uint8_t* Aq, const float* sA, const uint8_t* Bq, con
   if (!row_offsets) return E < 1 || E > kMaxExperts ? FP8Q_ERR_SHAPE : FP8Q_OK;
   return gemm_common(Aq, sA, Bq, sB, C, total_rows, N, K, out_dtype, 128, row_offsets, E,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fp8q_mx_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K <= 0 || K % 128 != 0) return 0;
+  return mx_scale_bytes(rows, K);
+}
+
+int fp8q_mx_quantize(const void* x, int in_dtype, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                     fp8q_stream_t stream) {
+  if (in_dtype != FP8Q_BF16 && in_dtype != FP8Q_FP32) return FP8Q_ERR_DTYPE;
+  if (rows < 0 || K <= 0 || K % 128 != 0) return FP8Q_ERR_SHAPE;
+  if (rows == 0) return FP8Q_OK;  // empty operands may carry null pointers
+  if (!x || !q || !s) return FP8Q_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return FP8Q_ERR_ALIGN;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  return in_dtype == FP8Q_FP32 ? launch_quant_mx<true>(x, rows, K, q, s, cs)
+                               : launch_quant_mx<false>(x, rows, K, q, s, cs);
+}
+
+int fp8q_mx_gemm(const uint8_t* Aq, const uint8_t* sA, const uint8_t* Bq, const uint8_t* sB, void* C, int64_t M,
+                 int64_t N, int64_t K, int out_dtype, fp8q_stream_t stream) {
+  return mx_gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8q_get_device_status(fp8q_stream_t stream) {

@@ -261,6 +261,59 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);    // M / 16
 }
 
+// ---------------------------------------------------------------------------
+// Block-scaled (MX) tensor-core operations
+// ---------------------------------------------------------------------------
+// Shared-memory descriptor of an unswizzled K-major matrix of 16-byte rows
+// stored back to back: 8-row x 16-byte core matrices, 128 bytes apart along
+// the rows.  This is the source of tcgen05.cp's 32x128b shape (32 rows x 16
+// bytes = 512 contiguous bytes); there is a single core-matrix column, so the
+// leading byte offset is never stepped over (it is set to the same 128).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address, bits 0-13
+  d |= static_cast<uint64_t>(128u >> 4) << 16;              // leading byte offset, bits 16-29
+  d |= static_cast<uint64_t>(128u >> 4) << 32;              // stride byte offset: next 8 rows, bits 32-45
+  d |= static_cast<uint64_t>(1u) << 46;                     // descriptor version for tcgen05, bits 46-47
+  return d;                                                 // bits 61-63 = 0: no swizzle
+}
+
+// tcgen05.cp 32x128b.warpx4: 32 rows x 16 bytes of shared memory into TMEM
+// columns [col, col + 4) of lanes 0-31, and the same copy into each of the
+// other three 32-lane quarters.  Issued by one thread; ordered before the
+// tcgen05.mma that this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor: kind::mxf8f6f4 with block scaling, A = B = E4M3,
+// UE8M0 scale factors, D = FP32, both operands K-major, dense, shape M x N.
+// `sf_id` selects the byte of each 32-bit scale-factor column that this
+// K = 32 step reads, for A and for B.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return (sf_id << 4)           // B scale-factor ID, bits 4-5
+         | (0u << 7)            // A format: E4M3
+         | (0u << 10)           // B format: E4M3
+         | ((N >> 3) << 17)     // N / 8
+         | (1u << 23)           // scale-factor type: UE8M0
+         | ((M >> 4) << 24)     // M / 16
+         | (sf_id << 29);       // A scale-factor ID, bits 29-30
+}
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T over one K = 32 step, E4M3 x
+// E4M3 -> FP32, one scale byte per row of A and per row of B (1x32 groups),
+// the scale factors read from TMEM.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Per-warpgroup register budget (all four warps of a warpgroup execute it).
 template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_dec() {

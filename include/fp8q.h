@@ -273,6 +273,57 @@ FP8Q_API int fp8q_gemm_unpromoted(const uint8_t *Aq, const uint8_t *Bq, float *C
                          int64_t M, int64_t N, int64_t K, fp8q_stream_t stream);
 
 /*
+ * MX (microscaling) variant.  The pages state that the fine-grained strategy
+ * follows the microscaling formats and that Blackwell tensor cores support
+ * those formats with smaller groups ("Deepseek Ai News Expert Interview", the
+ * DualPipe / microscaling paragraph).  Here: E4M3 codes in 1x32 groups along
+ * K, one power-of-two scale per group stored as an E8M0 byte, and a GEMM
+ * whose tensor cores apply those scales (no CUDA-core promotion).  Codes and
+ * scales are NOT comparable with the FP32-scale path above.
+ *
+ * Conversion of one group of 32 (the MX formats' own definition):
+ *   e = floor(log2(amax)) - 8, clamped to [-127, 127] (amax == 0: -127);
+ *   scale byte = e + 127;  code = E4M3_rn_satfinite(x / 2^e)  (the largest
+ *   elements of a group can saturate to +-448: x / 2^e < 512).
+ *
+ * Scale layout ("tiled"), for an operand of `rows` rows and K columns:
+ *   s[K/128][ceil(rows/128)][512] bytes; in the 512-byte chunk of row tile rt
+ *   and K-block kt, the scale of row 128*rt + r (r < 128) and 32-group
+ *   4*kt + c (c < 4) sits at byte (r % 32) * 16 + (r / 32) * 4 + c.  This is
+ *   the 32 x 16-byte matrix the tensor core's scale-factor copy consumes, so
+ *   the GEMM moves each chunk into tensor memory as is.  Rows past `rows` in
+ *   the last row tile hold byte 127 (scale 1).
+ */
+
+/* fp8q_mx_scale_bytes -- size in bytes of the tiled scale array of a
+ * rows x K operand: (K/128) * ceil(rows/128) * 512.  0 if rows < 0, K <= 0 or
+ * K % 128 != 0. */
+FP8Q_API size_t fp8q_mx_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * fp8q_mx_quantize -- MX quantization of x[rows][K] (row-major, BF16 or FP32)
+ * in 1x32 groups along K (activations and weights alike).
+ *   q   [rows][K] E4M3 codes;  s  tiled scales, fp8q_mx_scale_bytes(rows, K).
+ * rows >= 0 (any), K % 128 == 0.  x, q, s 16-byte aligned.  Codes and scale
+ * bytes are exact functions of x (bit-exact with the oracle).
+ */
+FP8Q_API int fp8q_mx_quantize(const void *x, int in_dtype, int64_t rows, int64_t K,
+                     uint8_t *q, uint8_t *s, fp8q_stream_t stream);
+
+/*
+ * fp8q_mx_gemm -- C[m][n] = sum_k (decode(Aq[m][k]) * 2^eA(m, k/32)) *
+ * (decode(Bq[n][k]) * 2^eB(n, k/32)), the scales applied by the tensor core
+ * (tcgen05.mma.kind::mxf8f6f4 with block scaling) and the whole K accumulated
+ * in its FP32 accumulator.
+ *   Aq [M][K], Bq [N][K] codes (K contiguous);  sA, sB tiled scales of each
+ *   (as written by fp8q_mx_quantize);  C [M][N] BF16 (RNE) or FP32.
+ * M >= 0 (any), N % 128 == 0, K % 128 == 0; pointers 16-byte aligned.
+ * Accuracy: |C - C_exact| <= 2e-3 * sum_k |a_dq * b_dq| (+ one BF16 rounding).
+ */
+FP8Q_API int fp8q_mx_gemm(const uint8_t *Aq, const uint8_t *sA, const uint8_t *Bq, const uint8_t *sB,
+                 void *C, int64_t M, int64_t N, int64_t K, int out_dtype, fp8q_stream_t stream);
+
+/*
  * fp8q_get_device_status -- synchronizes `stream`, then returns and clears
  * the current device's status word: FP8Q_OK, or FP8Q_ERR_TIMEOUT if a
  * kernel's bounded pipeline wait expired since the last call, or

@@ -92,3 +92,25 @@ def test_quantize_validation(lib):
     qg = lib.fp8q_quantize_act_gather
     assert qg(A, 0, 64, 128, NULL, 10, A, A, None) == 1
     assert qg(A, 0, 0, 128, A, 10, A, A, None) == 2                  # rows from an empty x
+
+
+def test_mx_validation(lib):
+    sb = lib.fp8q_mx_scale_bytes
+    assert sb(4096, 7168) == 56 * 32 * 512
+    assert sb(1, 128) == 512 and sb(129, 256) == 2 * 2 * 512 and sb(0, 128) == 0
+    assert sb(-1, 128) == 0 and sb(128, 100) == 0 and sb(128, 0) == 0
+    q = lib.fp8q_mx_quantize
+    assert q(NULL, 0, 128, 128, A, A, None) == 1
+    assert q(A, 0, 128, 128, NULL, A, None) == 1
+    assert q(A, 0, 128, 96, A, A, None) == 2                         # K % 128
+    assert q(A, 0, -1, 128, A, A, None) == 2
+    assert q(A, 3, 128, 128, A, A, None) == 4                        # dtype
+    assert q(A, 0, 128, 128, A, MIS, None) == 3
+    assert q(NULL, 0, 0, 128, NULL, NULL, None) == 0                 # empty
+    g = lib.fp8q_mx_gemm
+    assert g(NULL, A, A, A, A, 128, 128, 128, 0, None) == 1
+    assert g(A, A, A, A, A, 128, 100, 128, 0, None) == 2             # N % 128
+    assert g(A, A, A, A, A, 128, 128, 64, 0, None) == 2              # K % 128
+    assert g(A, A, A, A, A, 128, 128, 128, 5, None) == 4             # dtype
+    assert g(A, MIS, A, A, A, 128, 128, 128, 0, None) == 3
+    assert g(NULL, NULL, NULL, NULL, NULL, 0, 128, 128, 0, None) == 0  # empty
