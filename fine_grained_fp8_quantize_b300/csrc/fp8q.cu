@@ -338,10 +338,11 @@ int launch_quant_mx(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t*
     if (per_sm < 1) per_sm = 1;
     resident[dev].store(per_sm, std::memory_order_relaxed);
   }
-  const int64_t tiles = (K / 128) * ((rows + 127) / 128);
+  const int64_t slabs = (K / 128) * ((rows + 127) / 128) * 8;  // 16-row x 128-column slabs, one per warp
   const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
-  const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-  kern<<<grid, kMxQuantThreads, 0, stream>>>(x, rows, K, q, s, tiles);
+  const int64_t need = (slabs + kMxQuantThreads / 32 - 1) / (kMxQuantThreads / 32);
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  kern<<<grid, kMxQuantThreads, 0, stream>>>(x, rows, K, q, s, slabs);
   return launch_status();
 }
 

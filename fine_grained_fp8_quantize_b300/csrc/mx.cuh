@@ -35,80 +35,102 @@ namespace fp8q {
 // ---------------------------------------------------------------------------
 // Quantizer: 1x32 groups along K, E8M0 scales
 // ---------------------------------------------------------------------------
-// One 128 x 128 tile per CTA iteration (grid-stride over tiles), 256
-// threads.  Warp w holds rows 16w .. 16w+15; per step a warp reads two tile
-// rows (lanes 0-15 the first, 16-31 the second), each lane 8 consecutive
+// Work unit: a slab of 16 rows x 128 columns (one eighth of a 128 x 128
+// tile), one warp per slab, slabs striped over all warps of a persistent
+// grid; warps never wait for each other.  Per step a warp reads two slab rows
+// (lanes 0-15 the first, 16-31 the second), each lane 8 consecutive
 // elements, so one 32-element group spans 4 lanes and its amax is two
-// shuffles.  All eight steps' loads are issued before any arithmetic.
-// Codes leave as 8-byte stores (a half-warp writes one 128-byte row
-// segment); the tile's 512 scale bytes are gathered in shared memory and
-// leave as one 512-byte chunk.
+// shuffles.  All eight steps' loads are issued before any arithmetic.  Codes
+// leave as 8-byte stores (a half-warp writes one 128-byte row segment).  The
+// four scale bytes of one row in one K-block are adjacent in the tiled
+// layout, so they leave as one 4-byte store.
 constexpr int kMxQuantThreads = 256;
+
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+  const int b = static_cast<int>(__float_as_uint(amax) >> 23);  // amax >= 0: biased exponent
+  return static_cast<uint32_t>(b > 8 ? b - 8 : 0);
+}
 
 template <bool kF32>
 __global__ void __launch_bounds__(kMxQuantThreads)
     quant_mx_kernel(const void* __restrict__ x, int64_t rows, int64_t K, uint8_t* __restrict__ q,
-                    uint8_t* __restrict__ s, int64_t num_tiles) {
-  __shared__ __align__(16) uint8_t s_chunk[512];
-  const int warp = threadIdx.x >> 5;
+                    uint8_t* __restrict__ s, int64_t num_slabs) {
   const int lane = threadIdx.x & 31;
   const int64_t KT = K >> 7;
   const int64_t RT = (rows + 127) >> 7;
   const int half = lane >> 4;   // which of the two rows of a step
   const int col8 = lane & 15;   // 8-column slot within the row
-  const int grp = col8 >> 2;    // 32-group within the 128 columns
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kMxQuantThreads / 32);
 
-  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+  for (int64_t sl = static_cast<int64_t>(blockIdx.x) * (kMxQuantThreads / 32) + (threadIdx.x >> 5); sl < num_slabs;
+       sl += warps) {
+    const int64_t t = sl >> 3;        // tile
+    const int w = static_cast<int>(sl & 7);  // slab within the tile: rows 16w .. 16w+15
     const int64_t rt = t / KT;
     const int64_t kt = t - rt * KT;
     const int64_t col = kt * 128 + col8 * 8;
-    float v[8][8];
+    constexpr int kWords = kF32 ? 2 : 1;  // 16-byte words per lane per row
+    uint4 v[8][kWords];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int r = warp * 16 + 2 * i + half;
-      const int64_t m = rt * 128 + r;
+      const int64_t m = rt * 128 + w * 16 + 2 * i + half;
       if (m < rows) {
         if constexpr (kF32) {
-          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + m * K + col);
-          const float4 a = __ldg(p), b = __ldg(p + 1);
-          v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
-          v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
+          const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(x) + m * K + col);
+          v[i][0] = __ldg(p);
+          v[i][kWords - 1] = __ldg(p + 1);
         } else {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + m * K + col));
-          v[i][0] = bf16lo_to_f32(w.x); v[i][1] = bf16hi_to_f32(w.x);
-          v[i][2] = bf16lo_to_f32(w.y); v[i][3] = bf16hi_to_f32(w.y);
-          v[i][4] = bf16lo_to_f32(w.z); v[i][5] = bf16hi_to_f32(w.z);
-          v[i][6] = bf16lo_to_f32(w.w); v[i][7] = bf16hi_to_f32(w.w);
+          v[i][0] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + m * K + col));
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[i][j] = 0.f;
+        for (int j = 0; j < kWords; ++j) v[i][j] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int r = warp * 16 + 2 * i + half;
+      const int r = w * 16 + 2 * i + half;  // tile-local row
       const int64_t m = rt * 128 + r;
-      float amax = 0.f;
+      float e[8];
+      float amax;
+      if constexpr (kF32) {
+        e[0] = __uint_as_float(v[i][0].x); e[1] = __uint_as_float(v[i][0].y);
+        e[2] = __uint_as_float(v[i][0].z); e[3] = __uint_as_float(v[i][0].w);
+        e[4] = __uint_as_float(v[i][kWords - 1].x); e[5] = __uint_as_float(v[i][kWords - 1].y);
+        e[6] = __uint_as_float(v[i][kWords - 1].z); e[7] = __uint_as_float(v[i][kWords - 1].w);
+        amax = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(e[j]));
+      } else {
+        // packed BF16 |x| max (exact), then widen
+        const uint4 u = v[i][0];
+        const __nv_bfloat162 a2 = __hmax2(__hmax2(__habs2(bf2_of(u.x)), __habs2(bf2_of(u.y))),
+                                          __hmax2(__habs2(bf2_of(u.z)), __habs2(bf2_of(u.w))));
+        const uint32_t ab = u32_of(a2);
+        amax = fmaxf(bf16lo_to_f32(ab), bf16hi_to_f32(ab));
+        e[0] = bf16lo_to_f32(u.x); e[1] = bf16hi_to_f32(u.x);
+        e[2] = bf16lo_to_f32(u.y); e[3] = bf16hi_to_f32(u.y);
+        e[4] = bf16lo_to_f32(u.z); e[5] = bf16hi_to_f32(u.z);
+        e[6] = bf16lo_to_f32(u.w); e[7] = bf16hi_to_f32(u.w);
+      }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const int b = static_cast<int>(__float_as_uint(amax) >> 23);  // amax >= 0: biased exponent
-      const uint32_t byte = static_cast<uint32_t>(b > 8 ? b - 8 : 0);
-      const float inv = __uint_as_float((254u - byte) << 23);      // 2^-(byte - 127), a normal float
+      const uint32_t byte = mx_scale_byte(amax);
+      const float inv = __uint_as_float((254u - byte) << 23);  // 2^-(byte - 127), a normal float
+      // the row's four scale bytes (groups 0..3 sit on lanes 0, 4, 8, 12 of its half)
+      const int base = lane & 16;
+      const uint32_t word = __shfl_sync(0xffffffffu, byte, base) | (__shfl_sync(0xffffffffu, byte, base + 4) << 8) |
+                            (__shfl_sync(0xffffffffu, byte, base + 8) << 16) |
+                            (__shfl_sync(0xffffffffu, byte, base + 12) << 24);
       if (m < rows) {
-        const uint2 c = make_uint2(cvt_e4m3x4(v[i][0] * inv, v[i][1] * inv, v[i][2] * inv, v[i][3] * inv),
-                                   cvt_e4m3x4(v[i][4] * inv, v[i][5] * inv, v[i][6] * inv, v[i][7] * inv));
+        const uint2 c = make_uint2(cvt_e4m3x4(e[0] * inv, e[1] * inv, e[2] * inv, e[3] * inv),
+                                   cvt_e4m3x4(e[4] * inv, e[5] * inv, e[6] * inv, e[7] * inv));
         *reinterpret_cast<uint2*>(q + m * K + col) = c;
       }
-      if ((lane & 3) == 0)  // rows past the end get scale 1 (byte 127): defined, never read into C
-        s_chunk[(r & 31) * 16 + (r >> 5) * 4 + grp] = static_cast<uint8_t>(m < rows ? byte : 127u);
+      if (col8 == 0)  // rows past the end get scale 1 (byte 127): defined, never read into C
+        *reinterpret_cast<uint32_t*>(s + (kt * RT + rt) * 512 + (r & 31) * 16 + (r >> 5) * 4) =
+            m < rows ? word : 0x7F7F7F7Fu;
     }
-    __syncthreads();
-    if (threadIdx.x < 32)
-      reinterpret_cast<uint4*>(s + (kt * RT + rt) * 512)[threadIdx.x] = reinterpret_cast<const uint4*>(s_chunk)[threadIdx.x];
-    __syncthreads();
   }
 }
 

@@ -3,6 +3,8 @@
 // bounded pipeline waits, and the E4M3 / BF16 conversions.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 namespace fp8q {
@@ -370,6 +372,10 @@ __device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, f
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+
+// Bit casts between a word and two packed BF16 values.
+__device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
+__device__ __forceinline__ uint32_t u32_of(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

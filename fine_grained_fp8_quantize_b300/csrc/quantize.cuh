@@ -383,8 +383,6 @@ constexpr int kRcCodePitch = 144;             // bytes per row of a staged 128 x
 constexpr int kRcCodeBytes = 128 * kRcCodePitch;
 constexpr int kRcSmem = 2 * kRcTileBytes + 2 * kRcCodeBytes;  // inputs, row codes, transposed codes
 
-__device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
-__device__ __forceinline__ uint32_t u32_of(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
 // Shared memory of quant_rc_kernel<kRow, kCol>: two input tiles, then one
 // staged code tile per path.
