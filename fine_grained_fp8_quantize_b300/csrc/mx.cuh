@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(kMxQuantThreads)
 // 256 + 32 s (A: 4 columns, B: 8 columns at +16).  A stage's scale columns
 // are rewritten only after the MMAs that read them have completed: the
 // producer refills a stage after the MMAs' commit frees it.
+// Warps 0 and 1 run their loops as whole warps and issue from one elected
+// lane (elect.sync): the operands stay warp-uniform, which makes each issued
+// operation several times cheaper for the issuing thread than the same loop
+// run by lane 0 alone (measured: ~600 -> ~320 cycles per K-block).
 // Every mbarrier wait is bounded (mbar_wait); on expiry the kernel records a
 // timeout in the status word and unwinds.
 constexpr int kMxBM = 128;
@@ -231,21 +235,22 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        const int mt = t % args.tiles_m;
-        const int nt = t / args.tiles_m;
-        const bool full_n = static_cast<int64_t>(nt) * kMxBN + kMxBN <= args.N;
-        for (int64_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+    // the whole warp runs the loop; one elected lane issues the copies
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const int mt = t % args.tiles_m;
+      const int nt = t / args.tiles_m;
+      const bool full_n = static_cast<int64_t>(nt) * kMxBN + kMxBN <= args.N;
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_warp(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (elect_one()) {
           const uint32_t sf = sbase + kMxOffSf + stage * kMxSfBytes;
           mbar_arrive_expect_tx(bar_full + 8 * stage, kMxABytes + kMxBBytes + kMxSfBytes);
-          tma_load_2d(sbase + kMxOffA + stage * kMxABytes, &tmA, static_cast<int32_t>(kb * kMxBK),
-                      mt * kMxBM, bar_full + 8 * stage);
-          tma_load_2d(sbase + kMxOffB + stage * kMxBBytes, &tmB, static_cast<int32_t>(kb * kMxBK),
-                      nt * kMxBN, bar_full + 8 * stage);
+          tma_load_2d(sbase + kMxOffA + stage * kMxABytes, &tmA, static_cast<int32_t>(kb * kMxBK), mt * kMxBM,
+                      bar_full + 8 * stage);
+          tma_load_2d(sbase + kMxOffB + stage * kMxBBytes, &tmB, static_cast<int32_t>(kb * kMxBK), nt * kMxBN,
+                      bar_full + 8 * stage);
           bulk_load(sf, args.sA + (kb * args.tiles_m + mt) * 512, 512u, bar_full + 8 * stage);
           const uint8_t* sb = args.sB + (kb * rt_b + 2 * static_cast<int64_t>(nt)) * 512;
           if (full_n) {
@@ -256,57 +261,63 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             bulk_load(sf + 512, sb, 512u, bar_full + 8 * stage);
             bulk_load(sf + 1024, sb, 512u, bar_full + 8 * stage);
           }
-          ++issued;
-          if (++stage == kMxStages) { stage = 0; phase ^= 1u; }
         }
+        __syncwarp();
+        ++issued;
+        if (++stage == kMxStages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        // drain: wait (bounded) for the copies this thread still has in flight
-        for (uint32_t i = 0; i < kMxStages && i < issued; ++i) {
-          if (stage == 0) { stage = kMxStages; phase ^= 1u; }
-          --stage;
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar_full + 8 * stage, phase) && globaltimer_ns() - t0 < 1000000ull) {}
-        }
+    }
+    if (!ok && lane == 0) {
+      // drain: wait (bounded) for the copies still in flight
+      for (uint32_t i = 0; i < kMxStages && i < issued; ++i) {
+        if (stage == 0) { stage = kMxStages; phase ^= 1u; }
+        --stage;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_full + 8 * stage, phase) && globaltimer_ns() - t0 < 1000000ull) {}
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, tphase = 0;
-      bool ok = true, any = false;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        // the previous tile's accumulator has been read out
-        if (!mbar_wait(bar_tempty, tphase ^ 1u, abort_flag)) { ok = false; break; }
-        for (int64_t kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sf = sbase + kMxOffSf + stage * kMxSfBytes;
-          const uint32_t sfa = tmem_base + kMxSfCol0 + 32u * stage;
-          const uint32_t sfb = sfa + 16u;
+    // the whole warp runs the loop (operands stay warp-uniform); one elected
+    // lane issues the scale copies, the MMAs and the commits
+    uint32_t stage = 0, phase = 0, tphase = 0;
+    bool ok = true, any = false;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      // the previous tile's accumulator has been read out
+      if (!mbar_wait_warp(bar_tempty, tphase ^ 1u, abort_flag)) { ok = false; break; }
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_warp(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sf = sbase + kMxOffSf + stage * kMxSfBytes;
+        const uint32_t sfa = tmem_base + kMxSfCol0 + 32u * stage;
+        const uint32_t sfb = sfa + 16u;
+        const uint64_t adesc = smem_desc_k_sw128(sbase + kMxOffA + stage * kMxABytes);
+        const uint64_t bdesc = smem_desc_k_sw128(sbase + kMxOffB + stage * kMxBBytes);
+        if (elect_one()) {
           tmem_cp_32x128b_warpx4(sfa, smem_desc_rows16(sf));
           tmem_cp_32x128b_warpx4(sfb, smem_desc_rows16(sf + 512));
           tmem_cp_32x128b_warpx4(sfb + 4u, smem_desc_rows16(sf + 1024));
-          const uint64_t adesc = smem_desc_k_sw128(sbase + kMxOffA + stage * kMxABytes);
-          const uint64_t bdesc = smem_desc_k_sw128(sbase + kMxOffB + stage * kMxBBytes);
 #pragma unroll
           for (int k = 0; k < kMxBK / 32; ++k)
             mma_mxf8f6f4(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc_mx_e4m3(kMxBM, kMxBN, k), sfa, sfb,
                          (kb | k) != 0 ? 1u : 0u);
-          any = true;
           mma_commit(bar_empty + 8 * stage);
-          if (++stage == kMxStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        mma_commit(bar_tfull);
-        tphase ^= 1u;
+        __syncwarp();
+        any = true;
+        if (++stage == kMxStages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok && any) {
-        // drain: wait (bounded) until every MMA this thread issued is done
-        mma_commit(bar_drain);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < 1000000ull) {}
-      }
+      if (!ok) break;
+      if (elect_one()) mma_commit(bar_tfull);
+      __syncwarp();
+      tphase ^= 1u;
+    }
+    if (!ok && any && elect_one()) {
+      // drain: wait (bounded) until every MMA issued is done; the commit is
+      // made by the elected lane, the one that issued them
+      mma_commit(bar_drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < 1000000ull) {}
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int nt = t / args.tiles_m;
       const int64_t nh = static_cast<int64_t>(nt) * kMxBN + h * 128;
       const int64_t wrow0 = static_cast<int64_t>(mt) * kMxBM + q * 32;
-      if (!mbar_wait(bar_tfull, tphase, abort_flag)) break;
+      if (!mbar_wait_warp(bar_tfull, tphase, abort_flag)) break;
       tphase ^= 1u;
       __syncwarp();
       tc_fence_after();

@@ -31,6 +31,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// One lane of the (converged) warp returns true (elect.sync).  A loop that the
+// whole warp runs, issuing its tcgen05 / TMA operations from the elected
+// lane, keeps the operands warp-uniform; the same loop run by lane 0 alone
+// costs the issuing thread several times longer per operation.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
 // Release store / acquire load of a 32-bit flag at GPU scope.
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -125,6 +139,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+// The same wait made by a whole (converged) warp: every lane polls, and the
+// result is the warp's vote, so the warp never diverges on it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 
 // ---------------------------------------------------------------------------
