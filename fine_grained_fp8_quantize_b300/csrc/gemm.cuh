@@ -13,12 +13,13 @@
 // art, replaced by):
 //   warp 0       TMA producer: one 128x128 A tile + one 256x128 B tile per
 //                K-block into a kStages-deep ring of 128B-swizzled smem.
-//   warps 1-3    MMA issuers (warp 1 also owns TMEM): per K-block one
-//                thread issues four tcgen05.mma.kind::f8f6f4 (128x256x32)
-//                into a FRESH TMEM partial (the first with accumulate off);
-//                the three warps take K-blocks in turn.  Two partial buffers
-//                (2 x 256 FP32 columns = all 512) alternate, so the MMAs of
-//                block kb+1 overlap the promotion of block kb.
+//   warp 1       MMA issuer and TMEM owner: per K-block four
+//                tcgen05.mma.kind::f8f6f4 (128x256x32) into a FRESH TMEM
+//                partial (the first with accumulate off).  Two partial
+//                buffers (2 x 256 FP32 columns = all 512) alternate, so the
+//                MMAs of block kb+1 overlap the promotion of block kb.
+//                Warps 0 and 1 run their loops as whole warps and issue from
+//                one elected lane, which keeps the operands warp-uniform.
 //   warps 4..11  promotion + epilogue: each thread owns one row and 128
 //                columns of the 128x256 tile in 128 FP32 registers; per
 //                K-block it tcgen05.ld's its slice of the partial, frees the
@@ -53,7 +54,6 @@ constexpr uint32_t kBBytes = kBN * kBK;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
 
-constexpr int kMmaWarps = 3;              // warps 1..3 take turns issuing the MMAs
 constexpr int kSbRing = 8;                // per-column B-scale slices in flight
 constexpr uint32_t kSbSlotBytes = kBN * 4;  // one K-block's scales of a 256-column tile
 
@@ -151,10 +151,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t bar_empty = bar_full + kStages * 8;    // [kStages]
   const uint32_t bar_tfull = bar_empty + kStages * 8;   // [2]
   const uint32_t bar_tempty = bar_tfull + 2 * 8;        // [2]
-  const uint32_t bar_drain = bar_tempty + 2 * 8;        // [kMmaWarps]
-  const uint32_t bar_sfull = bar_drain + kMmaWarps * 8;  // [kSbRing]
+  const uint32_t bar_drain = bar_tempty + 2 * 8;        // [1]
+  const uint32_t bar_sfull = bar_drain + 8;             // [kSbRing]
   const uint32_t bar_sempty = bar_sfull + kSbRing * 8;  // [kSbRing]
-  const uint32_t bar_turn = bar_sempty + kSbRing * 8;   // [kMmaWarps]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* pref = reinterpret_cast<int*>(smem + kOffPref);
@@ -173,10 +172,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, 8);  // one arrive per promotion warp
     }
-    for (int w = 0; w < kMmaWarps; ++w) {
-      mbar_init(bar_drain + 8 * w, 1);
-      mbar_init(bar_turn + 8 * w, 1);  // arrived by the issuer of the previous K-block
-    }
+    mbar_init(bar_drain, 1);
     for (int r = 0; r < kSbRing; ++r) {
       mbar_init(bar_sfull + 8 * r, 1);
       mbar_init(bar_sempty + 8 * r, 8);  // one arrive per promotion warp
@@ -234,7 +230,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues the copies
+    {
       uint32_t stage = 0, phase = 0, issued = 0;
       uint32_t g = 0;  // K-blocks issued so far: position in the sB ring
       bool ok = true;
@@ -245,19 +242,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // that is not a multiple of 256 has 128 columns)
         const uint32_t sb_bytes = static_cast<uint32_t>(args.N - ti.n0 < kBN ? args.N - ti.n0 : kBN) * 4u;
         for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (kSbGran == 1) {
             const uint32_t slot = g % kSbRing, sph = (g / kSbRing) & 1u;
-            if (!mbar_wait(bar_sempty + 8 * slot, sph ^ 1u, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar_sfull + 8 * slot, sb_bytes);
-            bulk_load(sbase + kOffSB + slot * kSbSlotBytes, args.sB + kb * args.N + ti.n0, sb_bytes,
-                      bar_sfull + 8 * slot);
+            if (!mbar_wait_warp(bar_sempty + 8 * slot, sph ^ 1u, abort_flag)) { ok = false; break; }
+            if (elect_one()) {
+              mbar_arrive_expect_tx(bar_sfull + 8 * slot, sb_bytes);
+              bulk_load(sbase + kOffSB + slot * kSbSlotBytes, args.sB + kb * args.N + ti.n0, sb_bytes,
+                        bar_sfull + 8 * slot);
+            }
+            __syncwarp();
           }
-          mbar_arrive_expect_tx(bar_full + 8 * stage, kABytes + kBBytes);
-          tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, static_cast<int32_t>(kb * kBK),
-                      static_cast<int32_t>(ti.m0), bar_full + 8 * stage);
-          tma_load_2d(sbase + kOffB + stage * kBBytes, &tmB, static_cast<int32_t>(kb * kBK), ti.b_row,
-                      bar_full + 8 * stage);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar_full + 8 * stage, kABytes + kBBytes);
+            tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, static_cast<int32_t>(kb * kBK),
+                        static_cast<int32_t>(ti.m0), bar_full + 8 * stage);
+            tma_load_2d(sbase + kOffB + stage * kBBytes, &tmB, static_cast<int32_t>(kb * kBK), ti.b_row,
+                        bar_full + 8 * stage);
+          }
+          __syncwarp();
           ++issued;
           ++g;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -276,8 +279,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           it += hi - lo;
         }
       }
-      if (!ok) {
-        // drain: wait (bounded) for the copies this thread still has in flight
+      if (!ok && lane == 0) {
+        // drain: wait (bounded) for the copies still in flight
         for (uint32_t i = 0; i < kStages && i < issued; ++i) {
           if (stage == 0) { stage = kStages; phase ^= 1u; }
           --stage;
@@ -294,63 +297,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp <= kMmaWarps) {
-    // ------------------------------------------------------------ MMA issuers
-    // K-block g of this CTA's sequence is issued by warp 1 + g % 3.  A
-    // thread whose tcgen05.mma waits for room in the tensor pipe holds up the
-    // other warps of its scheduler; rotating the issue over three schedulers
-    // spreads that cost instead of slowing one quarter of the promotion rows.
-    // The issuers still go strictly in K-block order: the issuer of g waits
-    // for its turn (bar_turn, arrived by the issuer of g-1) before it waits
-    // on the ring barriers, so no barrier is ever waited on more than one
-    // phase ahead.
-    if (lane == 0) {
-      const uint32_t w = static_cast<uint32_t>(warp - 1);
-      uint64_t total;  // K-blocks of this CTA
-      if constexpr (kStreamK) {
-        const int64_t all = static_cast<int64_t>(num_tiles) * KB;
-        total = static_cast<uint64_t>(streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x) -
-                                      streamk_begin(all, blockIdx.x, gridDim.x));
-      } else {
-        const int64_t local_tiles =
-            blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
-      }
-      bool ok = true, any = false;
-      uint32_t turn = 0;  // turns this thread has taken
-      for (uint64_t g = w; g < total; g += kMmaWarps, ++turn) {
-        if (g > 0) {
-          // phase index of this turn on bar_turn[w]: warp 1 takes g = 0 without waiting
-          const uint32_t ph = (turn - (w == 0 ? 1u : 0u)) & 1u;
-          if (!mbar_wait(bar_turn + 8 * w, ph, abort_flag)) { ok = false; break; }
-        }
-        const uint32_t stage = static_cast<uint32_t>(g % kStages);
-        const uint32_t phase = static_cast<uint32_t>(g / kStages) & 1u;
-        const uint32_t buf = static_cast<uint32_t>(g & 1u);
-        const uint32_t bphase = static_cast<uint32_t>(g >> 1) & 1u;
-        if (!mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t adesc = smem_desc_k_sw128(sbase + kOffA + stage * kABytes);
-        const uint64_t bdesc = smem_desc_k_sw128(sbase + kOffB + stage * kBBytes);
-        const uint32_t d = tmem_base + buf * kBN;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop, so descriptors and addresses stay
+    // warp-uniform; one elected lane issues the MMAs and the commits.
+    // (Issued from lane 0 alone, the same loop cost the issuing thread about
+    // twice as long per K-block, longer than the K-block's MMAs take.)
+    uint64_t total;  // K-blocks of this CTA
+    if constexpr (kStreamK) {
+      const int64_t all = static_cast<int64_t>(num_tiles) * KB;
+      total = static_cast<uint64_t>(streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x) -
+                                    streamk_begin(all, blockIdx.x, gridDim.x));
+    } else {
+      const int64_t local_tiles =
+          blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
+    }
+    bool ok = true, any = false;
+    for (uint64_t g = 0; g < total; ++g) {
+      const uint32_t stage = static_cast<uint32_t>(g % kStages);
+      const uint32_t phase = static_cast<uint32_t>(g / kStages) & 1u;
+      const uint32_t buf = static_cast<uint32_t>(g & 1u);
+      const uint32_t bphase = static_cast<uint32_t>(g >> 1) & 1u;
+      if (!mbar_wait_warp(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t adesc = smem_desc_k_sw128(sbase + kOffA + stage * kABytes);
+      const uint64_t bdesc = smem_desc_k_sw128(sbase + kOffB + stage * kBBytes);
+      const uint32_t d = tmem_base + buf * kBN;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < kBK / 32; ++k) {
           // K-slice k of the 128-byte swizzled rows: +32 bytes = +2 in the
           // descriptor's 16-byte address units
           mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
         }
-        any = true;
         mma_commit(bar_empty + 8 * stage);
         mma_commit(bar_tfull + 8 * buf);
-        mbar_arrive(bar_turn + 8 * ((w + 1) % kMmaWarps));  // the next K-block's issuer may go
       }
-      if (!ok && any) {
-        // drain: wait (bounded) until every MMA this thread issued is done
-        mma_commit(bar_drain + 8 * w);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_drain + 8 * w, 0) && globaltimer_ns() - t0 < 1000000ull) {}
-      }
+      __syncwarp();
+      any = true;
+    }
+    if (!ok && any && elect_one()) {
+      // drain: wait (bounded) until every MMA issued is done; the commit is
+      // made by the elected lane, the one that issued them
+      mma_commit(bar_drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_drain, 0) && globaltimer_ns() - t0 < 1000000ull) {}
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ promotion
@@ -394,10 +387,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t slot = 0;
         if constexpr (kSbGran == 1) {
           slot = g % kSbRing;
-          if (!mbar_wait(bar_sfull + 8 * slot, (g / kSbRing) & 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(bar_sfull + 8 * slot, (g / kSbRing) & 1u, abort_flag)) { ok = false; break; }
           sbs = reinterpret_cast<const float4*>(smem + kOffSB + slot * kSbSlotBytes) + h * 32;
         }
-        if (!mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(bar_tfull + 8 * buf, bphase, abort_flag)) { ok = false; break; }
         __syncwarp();
         tc_fence_after();
         const uint32_t taddr = tmem_base + t_lane + buf * kBN + h * 128;
