@@ -244,6 +244,21 @@ def check_status(f, when):
         raise RuntimeError("device status %s: %s" % (when, f.fp8q_status_string(st)))
 
 
+def max_over_ranks(torch, ms, dist, device):
+    """The slowest rank's timed-region duration (every rank gets it)."""
+    if not dist:
+        return ms
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def replica_value(world, flops_per_step, steps, ms):
+    """Whole-job TFLOP/s of `world` independent replicas, each running
+    `steps` steps of `flops_per_step`, timed by the slowest rank (ms)."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def run_timed(torch, stream, step, steps, warmup, dist=None):
     """Warm-up, then exactly `steps` steps bracketed by barrier + synchronize,
     with clocks sampled during the timed region.  -> (ms total, clocks)."""
@@ -292,11 +307,8 @@ def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
 
     ms, clocks = run_timed(torch, stream, step, args.steps, args.warmup, dist)
     check_status(f, "after the fprop timing")
-    if dist:
-        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * flops * args.steps / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(torch, ms, dist, "cuda")
+    value = replica_value(world, flops, args.steps, ms)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
