@@ -64,12 +64,14 @@ def _load():
     L.fp8q_mx_scale_bytes.restype = ctypes.c_size_t
     L.fp8q_mx_quantize.argtypes = [P, I32, I64, I64, P, P, P]
     L.fp8q_mx_gemm.argtypes = [P, P, P, P, P, I64, I64, I64, I32, P]
+    L.fp8q_selftest_wait_timeout.argtypes = [P]
     L.fp8q_get_device_status.argtypes = [P]
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [I32]
     for name in ("fp8q_quantize_act", "fp8q_quantize_act_gather", "fp8q_quantize_weight",
                  "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_ws_static",
                  "fp8q_gemm_unpromoted", "fp8q_grouped_gemm", "fp8q_mx_quantize", "fp8q_mx_gemm",
+                 "fp8q_selftest_wait_timeout",
                  "fp8q_get_device_status", "fp8q_version"):
         getattr(L, name).restype = I32
     return L
@@ -243,6 +245,12 @@ def fp8q_mx_gemm(Aq, sA, Bq, sB, C, stream=None):
         raise ValueError("scale buffer smaller than fp8q_mx_scale_bytes")
     _check("fp8q_mx_gemm", _lib.fp8q_mx_gemm(_ptr(Aq), _ptr(sA), _ptr(Bq), _ptr(sB), _ptr(C), M, N, K,
                                              _out_dtype(C), _stream(stream)))
+
+
+def fp8q_selftest_wait_timeout(stream=None):
+    """Failure-detection self-test: a kernel whose bounded wait expires
+    (about 2 s); afterwards fp8q_get_device_status() reports the timeout."""
+    _check("fp8q_selftest_wait_timeout", _lib.fp8q_selftest_wait_timeout(_stream(stream)))
 
 
 def fp8q_get_device_status(stream=None):

@@ -119,4 +119,21 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// Failure-detection self-test.  One thread waits on an mbarrier that nothing
+// ever arrives on, through mbar_wait, the bounded wait every pipeline of this
+// library uses.  The wait gives up after its limit (kWaitTimeoutNs), records
+// FP8Q_ERR_TIMEOUT in the device status word and returns false, and the
+// kernel ends normally: nothing traps, faults or hangs, and the context stays
+// usable.
+__global__ void selftest_wait_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_word = 0;
+    fence_mbar_init();
+    (void)mbar_wait(smem_u32(&bar), 0, &abort_word);  // phase 0 never completes
+  }
+}
+
 }  // namespace fp8q

@@ -623,6 +623,13 @@ int fp8q_mx_gemm(const uint8_t* Aq, const uint8_t* sA, const uint8_t* Bq, const 
   return mx_gemm_common(Aq, sA, Bq, sB, C, M, N, K, out_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fp8q_selftest_wait_timeout(fp8q_stream_t stream) {
+  const int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  return launch_status();
+}
+
 int fp8q_get_device_status(fp8q_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8Q_ERR_CUDA;
   unsigned int v = 0;

@@ -324,6 +324,17 @@ FP8Q_API int fp8q_mx_gemm(const uint8_t *Aq, const uint8_t *sA, const uint8_t *B
                  void *C, int64_t M, int64_t N, int64_t K, int out_dtype, fp8q_stream_t stream);
 
 /*
+ * fp8q_selftest_wait_timeout -- failure-detection self-test, not part of the
+ * method.  Launches one thread that waits on an mbarrier nothing arrives on,
+ * through the same bounded wait the GEMM and quantizer pipelines use.  After
+ * the wait limit (2 s) the kernel records FP8Q_ERR_TIMEOUT in the device
+ * status word and ends normally (no trap, no fault, no hang); the next
+ * fp8q_get_device_status(stream) returns FP8Q_ERR_TIMEOUT and clears it, and
+ * the CUDA context stays usable.  Returns the launch status.
+ */
+FP8Q_API int fp8q_selftest_wait_timeout(fp8q_stream_t stream);
+
+/*
  * fp8q_get_device_status -- synchronizes `stream`, then returns and clears
  * the current device's status word: FP8Q_OK, or FP8Q_ERR_TIMEOUT if a
  * kernel's bounded pipeline wait expired since the last call, or
