@@ -168,9 +168,17 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
     if (per_sm < 1) per_sm = 1;
     resident[dev].store(per_sm, std::memory_order_relaxed);
   }
+  // the code tiles leave through TMA stores (128-byte swizzle, 128 x 128 boxes)
+  CUtensorMap tm_row, tm_col;
+  std::memset(&tm_row, 0, sizeof(tm_row));
+  std::memset(&tm_col, 0, sizeof(tm_col));
+  if (kRow && !make_tmap_u8(&tm_row, a.q_row, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M), 128))
+    return FP8Q_ERR_CUDA;
+  if (kCol && !make_tmap_u8(&tm_col, a.q_colT, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), 128))
+    return FP8Q_ERR_CUDA;
   const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-  kern<<<grid, kThreads, kSmem, stream>>>(a, tiles);
+  kern<<<grid, kThreads, kSmem, stream>>>(a, tiles, tm_row, tm_col);
   return launch_status();
 }
 

@@ -19,6 +19,7 @@
 // 16-byte transposed stores (a warp writes full 32-byte sectors).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -350,6 +351,8 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
     // quant_tile_body neither stores nor reduces rows >= M
     quant_tile_body<false, kMode>(f, args, t % kbt, t / kbt, sm);
   }
+  // the code tiles' stores have completed before the CTA exits
+  if (tid == 0 || tid == 128) bulk_wait_all();
   if (t < num_tiles) {
     // a wait failed: let every copy this CTA issued land before it exits
     // (bounded; the status word already records the timeout)
@@ -371,29 +374,36 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
 //   warps 4-7  column path: thread (p, h) owns columns 2p, 2p+1 over the
 //              64 rows of half h (64 x 4-byte reads); the two halves meet in
 //              shared memory for the 128x1 amax.
-// Each path writes its 128 x 128 codes into a staged shared-memory tile and
-// then copies it out with whole 128-byte lines per 8 lanes, so every global
-// store instruction writes full sectors.  The padded pitches keep the
-// shared-memory reads and writes near conflict-free.  The amax is exact in
-// BF16; the scale and cast are those of quant_tile_body.
+// Each path writes its 128 x 128 codes into a staged shared-memory tile in
+// the 128-byte-swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8),
+// which keeps those writes conflict-free) and one thread stores the tile
+// with a single TMA store (whole lines; rows past M are clipped).  The store
+// must have read the tile before the next tile is staged: its issuer waits
+// for that just before the CTA barrier every tile passes anyway.  The amax
+// is exact in BF16; the scale and cast are those of quant_tile_body.
 // ---------------------------------------------------------------------------
 constexpr int kRcPitch = 272;                 // bytes per smem tile row
 constexpr int kRcTileBytes = 128 * kRcPitch;  // one tile buffer
-constexpr int kRcCodePitch = 144;             // bytes per row of a staged 128 x 128 code tile
+constexpr int kRcCodePitch = 128;             // bytes per row of a staged (swizzled) 128 x 128 code tile
 constexpr int kRcCodeBytes = 128 * kRcCodePitch;
 constexpr int kRcSmem = 2 * kRcTileBytes + 2 * kRcCodeBytes;  // inputs, row codes, transposed codes
 
 
 // Shared memory of quant_rc_kernel<kRow, kCol>: two input tiles, then one
-// staged code tile per path.
+// staged code tile per path (+ slack to align the base to 1024 bytes, the
+// 128-byte swizzle's period; the tile buffers are multiples of 1024 bytes).
 constexpr int rc_smem_bytes(bool row, bool col) {
-  return 2 * kRcTileBytes + ((row ? 1 : 0) + (col ? 1 : 0)) * kRcCodeBytes;
+  return 2 * kRcTileBytes + ((row ? 1 : 0) + (col ? 1 : 0)) * kRcCodeBytes + 1024;
 }
+static_assert(kRcTileBytes % 1024 == 0 && kRcCodeBytes % 1024 == 0, "staged tiles must stay 1024-aligned");
 
 template <bool kRow, bool kCol>
 __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
-    quant_rc_kernel(const QuantArgs args, int64_t num_tiles) {
-  extern __shared__ __align__(128) uint8_t rsm[];  // [2][128][kRcPitch] inputs, then the staged code tiles
+    quant_rc_kernel(const QuantArgs args, int64_t num_tiles, const __grid_constant__ CUtensorMap tm_row,
+                    const __grid_constant__ CUtensorMap tm_col) {
+  extern __shared__ __align__(128) uint8_t rsm_raw[];
+  // [2][128][kRcPitch] inputs, then the staged code tiles
+  uint8_t* rsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~uintptr_t(1023));
   __shared__ float s_cmax[2][128];                 // column maxima of each 64-row half
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ int abort_word;
@@ -480,7 +490,10 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     }
     const int64_t tn = t + 2 * static_cast<int64_t>(gridDim.x);
     if (ok && tid == 0 && tn < num_tiles) mbar_arrive_expect_tx(bar0 + 8 * b, tile_bytes(tn));
-    // every thread has its values (buffer b is free) or some wait failed
+    // each path's store issuer: the previous tile's store has read its staged codes
+    if (tid == 0 || tid == 128) bulk_wait_read<0>();
+    // every thread has its values (buffer b is free), the staged code tiles
+    // are free, or some wait failed
     if (__syncthreads_or(!ok)) break;
     if (tid < 128 && tn < num_tiles) issue_row(tn, b);
 
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
       float sc, inv;
       group_scale(fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), sc, inv);
       if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
-      uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);
+      uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);  // row tid
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
         uint32_t c[4];
@@ -504,17 +517,13 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
           c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
                             bf16hi_to_f32(bb) * inv);
         }
-        st[i >> 1] = make_uint4(c[0], c[1], c[2], c[3]);
+        st[(i >> 1) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);
       }
+      fence_proxy_async_smem();
       asm volatile("bar.sync 3, 128;" ::: "memory");
-      // copy out: 8 lanes per 128-byte row, 4 rows per instruction
-      const int warp = tid >> 5, lane = tid & 31;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = warp * 32 + j * 4 + (lane >> 3);
-        const int64_t mr = m0 + r;
-        const uint4 q = *reinterpret_cast<const uint4*>(rsm + 2 * kRcTileBytes + r * kRcCodePitch + (lane & 7) * 16);
-        if (mr < M) *reinterpret_cast<uint4*>(args.q_row + mr * K + k0 + (lane & 7) * 16) = q;
+      if (tid == 0) {
+        tma_store_2d(&tm_row, smem_u32(rsm + 2 * kRcTileBytes), static_cast<int32_t>(k0), static_cast<int32_t>(m0));
+        bulk_commit();
       }
     } else if constexpr (kCol) {
       // ---- 128x1 column groups of columns k0 + 2p, k0 + 2p + 1
@@ -531,8 +540,8 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
       if (hh == 0) *reinterpret_cast<float2*>(args.s_col + mb * K + k0 + 2 * p) = make_float2(sc0, sc1);
       // staged transposed tile: row = column of x, 128 token bytes per row
       uint8_t* ct = rsm + 2 * kRcTileBytes + (kRow ? kRcCodeBytes : 0);
-      uint4* d0 = reinterpret_cast<uint4*>(ct + (2 * p) * kRcCodePitch + hh * 64);
-      uint4* d1 = reinterpret_cast<uint4*>(ct + (2 * p + 1) * kRcCodePitch + hh * 64);
+      uint4* d0 = reinterpret_cast<uint4*>(ct + (2 * p) * kRcCodePitch);
+      uint4* d1 = reinterpret_cast<uint4*>(ct + (2 * p + 1) * kRcCodePitch);
 #pragma unroll
       for (int r = 0; r < 64; r += 16) {
         uint32_t c0[4], c1[4];
@@ -544,20 +553,20 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
           c1[u] = cvt_e4m3x4(bf16hi_to_f32(a) * inv1, bf16hi_to_f32(bb) * inv1, bf16hi_to_f32(cc) * inv1,
                              bf16hi_to_f32(dd) * inv1);
         }
-        d0[r >> 4] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-        d1[r >> 4] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+        // token chunk hh * 4 + r / 16 of rows 2p and 2p+1, swizzled
+        d0[(hh * 4 + (r >> 4)) ^ ((2 * p) & 7)] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+        d1[(hh * 4 + (r >> 4)) ^ ((2 * p + 1) & 7)] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
       }
+      fence_proxy_async_smem();
       asm volatile("bar.sync 2, 128;" ::: "memory");
-      // copy out: 8 lanes per 128-byte row of the transposed output
-      const int cw = ctid >> 5, lane = tid & 31;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = cw * 32 + j * 4 + (lane >> 3);
-        const uint4 q = *reinterpret_cast<const uint4*>(ct + r * kRcCodePitch + (lane & 7) * 16);
-        *reinterpret_cast<uint4*>(args.q_colT + (k0 + r) * M + m0 + (lane & 7) * 16) = q;
+      if (ctid == 0) {
+        tma_store_2d(&tm_col, smem_u32(ct), static_cast<int32_t>(m0), static_cast<int32_t>(k0));
+        bulk_commit();
       }
     }
   }
+  // the code tiles' stores have completed before the CTA exits
+  if (tid == 0 || tid == 128) bulk_wait_all();
   if (t < num_tiles) {
     // a wait failed: let every copy this CTA issued land before it exits
     for (uint32_t d = 0; d < 2; ++d) {
