@@ -182,14 +182,40 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   return launch_status();
 }
 
+// BF16 rows only (and the row gather): one warp per 16-row slab, as many
+// CTAs as fit on the device at once (occupancy probed once per device).
+int launch_quant_rows(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
+  static std::atomic<int> resident[64];
+  DeviceInfo di;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  const int st = check_device(&di);
+  if (st != FP8Q_OK) return st;
+  int per_sm = resident[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_rows_kernel, kRowsThreads, 0) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t slabs = tiles * 8;
+  const int64_t need = (slabs + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
+  const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  quant_rows_kernel<<<grid, kRowsThreads, 0, stream>>>(a, slabs);
+  return launch_status();
+}
+
 // FP32 input: one CTA per tile.  BF16 rows + transposed columns: the
-// split-role kernel (both paths busy).  Other BF16 modes (one path, or
-// 128x128 blocks): the pipelined kernel, which keeps 12 warps per SM where a
-// one-path split-role CTA would keep 8 (measured faster).
+// split-role kernel (both paths busy).  BF16 rows only: one warp per 16-row
+// slab.  Other BF16 modes (columns only, or 128x128 blocks): the pipelined
+// kernel, which keeps 12 warps per SM where a one-path split-role CTA would
+// keep 8 (measured faster).
 template <int kMode>
 int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cudaStream_t s) {
   if (in_dtype == FP8Q_FP32) return launch_quant<true, kMode>(a, gx, gy, s);
   if constexpr (kMode == (kQRow | kQCol)) return launch_quant_rc<true, true>(a, gx * gy, s);
+  if constexpr (kMode == kQRow) return launch_quant_rows(a, gx * gy, s);
   return launch_quant_pipe<kMode>(a, gx * gy, s);
 }
 

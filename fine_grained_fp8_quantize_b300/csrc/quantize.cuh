@@ -578,4 +578,70 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// quant_rows_kernel: BF16 input, 1x128 row groups only (optionally through
+// the row gather).  The work unit is a slab of 16 rows x 128 columns, one warp
+// per slab, slabs striped over all warps of a persistent grid; warps never
+// wait for each other.  Per step a warp reads two rows (lanes 0-15 the first,
+// 16-31 the second), each lane 8 consecutive values with one 16-byte load, so
+// a row's amax is a packed BF16 max (exact) and four shuffles among its 16
+// lanes.  All eight steps' loads are in flight before any arithmetic.  Codes
+// leave as 8-byte stores (a half-warp writes one 128-byte row segment); each
+// row's scale is one 4-byte store.  The scale and cast are those of
+// quant_tile_body, so the codes are the same bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kRowsThreads = 256;
+
+__global__ void __launch_bounds__(kRowsThreads) quant_rows_kernel(const QuantArgs args, int64_t num_slabs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t K = args.K;
+  const int64_t M = args.M;
+  const int64_t KT = K >> 7;
+  const int half = lane >> 4;  // which of the two rows of a step
+  const int col8 = lane & 15;  // 8-column slot within the row
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsThreads / 32);
+  for (int64_t sl = static_cast<int64_t>(blockIdx.x) * (kRowsThreads / 32) + (threadIdx.x >> 5); sl < num_slabs;
+       sl += warps) {
+    const int64_t t = sl >> 3;
+    const int w = static_cast<int>(sl & 7);  // rows 16w .. 16w+15 of the tile
+    const int64_t rt = t / KT;
+    const int64_t kt = t - rt * KT;
+    const int64_t col = kt * 128 + col8 * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t m = rt * 128 + w * 16 + 2 * i + half;
+      if (m < M) {
+        const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(__ldg(args.src_rows + m)) : m;
+        v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(args.x) + src * K + col));
+      } else {
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t m = rt * 128 + w * 16 + 2 * i + half;
+      const uint4 u = v[i];
+      const __nv_bfloat162 a2 = __hmax2(__hmax2(__habs2(bf2_of(u.x)), __habs2(bf2_of(u.y))),
+                                        __hmax2(__habs2(bf2_of(u.z)), __habs2(bf2_of(u.w))));
+      const uint32_t ab = u32_of(a2);
+      float amax = fmaxf(bf16lo_to_f32(ab), bf16hi_to_f32(ab));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      float sc, inv;
+      group_scale(amax, sc, inv);
+      if (m < M) {
+        const uint2 c = make_uint2(
+            cvt_e4m3x4(bf16lo_to_f32(u.x) * inv, bf16hi_to_f32(u.x) * inv, bf16lo_to_f32(u.y) * inv,
+                       bf16hi_to_f32(u.y) * inv),
+            cvt_e4m3x4(bf16lo_to_f32(u.z) * inv, bf16hi_to_f32(u.z) * inv, bf16lo_to_f32(u.w) * inv,
+                       bf16hi_to_f32(u.w) * inv));
+        *reinterpret_cast<uint2*>(args.q_row + m * K + col) = c;
+        if (col8 == 0) args.s_row[kt * args.ld_srow + m] = sc;
+      }
+    }
+  }
+}
+
 }  // namespace fp8q
