@@ -580,8 +580,8 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
 
 
 // ---------------------------------------------------------------------------
-// quant_rows_kernel: BF16 input, 1x128 row groups only (optionally through
-// the row gather).  The work unit is a slab of 16 rows x 128 columns, one warp
+// quant_rows_kernel: BF16 input, 1x128 row groups only (it supports the row
+// gather; the library routes gathered rows to quant_pipe_kernel, faster there).  The work unit is a slab of 16 rows x 128 columns, one warp
 // per slab, slabs striped over all warps of a persistent grid; warps never
 // wait for each other.  Per step a warp reads two rows (lanes 0-15 the first,
 // 16-31 the second), each lane 8 consecutive values with one 16-byte load, so
