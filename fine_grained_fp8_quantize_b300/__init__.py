@@ -25,8 +25,9 @@ __all__ = [
     "fp8q_quantize_weight_ex", "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_ws", "fp8q_gemm_workspace_size",
     "fp8q_gemm_ws_static", "fp8q_gemm_unpromoted",
     "fp8q_grouped_gemm", "gemm_workspace",
+    "fp8q_mx_scale_bytes", "fp8q_mx_quantize", "fp8q_mx_gemm", "fp8q_selftest_wait_timeout",
     "fp8q_get_device_status", "fp8q_status_string", "fp8q_version",
-    "quantize_act", "quantize_act_gather", "quantize_weight", "gemm", "grouped_gemm",
+    "quantize_act", "quantize_act_gather", "quantize_weight", "gemm", "grouped_gemm", "mx_quantize", "mx_gemm",
 ]
 
 FP8Q_BF16 = 0
