@@ -94,6 +94,21 @@ bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
+// 2-D BF16 input [rows][cols] (cols contiguous), box 128 columns (256 bytes)
+// x 128 rows, dense (no swizzle).  Out-of-range elements read as zero.
+bool make_tmap_bf16_tile(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {128u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D output tensor C [rows][cols] (BF16 or FP32, cols contiguous) for TMA
 // stores of 32-row x 32-byte boxes, no swizzle.
 bool make_tmap_out(CUtensorMap* tm, void* base, bool f32, uint64_t cols, uint64_t rows) {
@@ -169,16 +184,18 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
     resident[dev].store(per_sm, std::memory_order_relaxed);
   }
   // the code tiles leave through TMA stores (128-byte swizzle, 128 x 128 boxes)
-  CUtensorMap tm_row, tm_col;
+  CUtensorMap tm_x, tm_row, tm_col;
   std::memset(&tm_row, 0, sizeof(tm_row));
   std::memset(&tm_col, 0, sizeof(tm_col));
+  if (!make_tmap_bf16_tile(&tm_x, a.x, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)))
+    return FP8Q_ERR_CUDA;
   if (kRow && !make_tmap_u8(&tm_row, a.q_row, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M), 128))
     return FP8Q_ERR_CUDA;
   if (kCol && !make_tmap_u8(&tm_col, a.q_colT, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), 128))
     return FP8Q_ERR_CUDA;
   const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-  kern<<<grid, kThreads, kSmem, stream>>>(a, tiles, tm_row, tm_col);
+  kern<<<grid, kThreads, kSmem, stream>>>(a, tiles, tm_x, tm_row, tm_col);
   return launch_status();
 }
 

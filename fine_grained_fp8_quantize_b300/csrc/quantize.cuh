@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
 // for that just before the CTA barrier every tile passes anyway.  The amax
 // is exact in BF16; the scale and cast are those of quant_tile_body.
 // ---------------------------------------------------------------------------
-constexpr int kRcPitch = 272;                 // bytes per smem tile row
+constexpr int kRcPitch = 256;                 // bytes per smem tile row (one dense TMA box)
 constexpr int kRcTileBytes = 128 * kRcPitch;  // one tile buffer
 constexpr int kRcCodePitch = 128;             // bytes per row of a staged (swizzled) 128 x 128 code tile
 constexpr int kRcCodeBytes = 128 * kRcCodePitch;
@@ -399,8 +399,8 @@ static_assert(kRcTileBytes % 1024 == 0 && kRcCodeBytes % 1024 == 0, "staged tile
 
 template <bool kRow, bool kCol>
 __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
-    quant_rc_kernel(const QuantArgs args, int64_t num_tiles, const __grid_constant__ CUtensorMap tm_row,
-                    const __grid_constant__ CUtensorMap tm_col) {
+    quant_rc_kernel(const QuantArgs args, int64_t num_tiles, const __grid_constant__ CUtensorMap tm_x,
+                    const __grid_constant__ CUtensorMap tm_row, const __grid_constant__ CUtensorMap tm_col) {
   extern __shared__ __align__(128) uint8_t rsm_raw[];
   // [2][128][kRcPitch] inputs, then the staged code tiles
   uint8_t* rsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~uintptr_t(1023));
@@ -416,23 +416,14 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   const uint32_t bar0 = smem_u32(&bars[0]);
   const uint32_t buf0 = smem_u32(rsm);
 
-  // bytes that land for tile tt (rows past M are not copied)
-  // (with column groups every tile is full and rows are not gathered)
-  auto tile_bytes = [&](int64_t tt) -> uint32_t {
-    if constexpr (kCol) return 128u * 256u;
-    const int64_t rows = M - (tt / kbt) * 128;
-    return static_cast<uint32_t>(rows < 128 ? rows : 128) * 256u;
-  };
-  auto issue_row = [&](int64_t tt, int b) {  // threads 0..127: tile row tid, through the row gather
-    const int64_t m = (tt / kbt) * 128 + tid;
-    if constexpr (kCol) {
-      bulk_load(buf0 + b * kRcTileBytes + tid * kRcPitch,
-                static_cast<const uint16_t*>(args.x) + m * K + (tt % kbt) * 128, 256u, bar0 + 8 * b);
-    } else if (m < M) {
-      const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(args.src_rows[m]) : m;
-      bulk_load(buf0 + b * kRcTileBytes + tid * kRcPitch,
-                static_cast<const uint16_t*>(args.x) + src * K + (tt % kbt) * 128, 256u, bar0 + 8 * b);
-    }
+  // Input tile tt: one TMA load of 128 rows x 128 columns (256-byte rows,
+  // dense, no swizzle).  The row path reads its row's 16-byte chunks in a
+  // rotated order, which keeps those reads free of bank conflicts.
+  static_assert(kCol, "the TMA-fed rows+columns kernel needs column groups (M % 128 == 0, no row gather)");
+  auto tile_bytes = [&](int64_t) -> uint32_t { return static_cast<uint32_t>(kRcTileBytes); };
+  auto issue_tile = [&](int64_t tt, int b) {  // one thread
+    tma_load_2d(buf0 + b * kRcTileBytes, &tm_x, static_cast<int32_t>((tt % kbt) * 128),
+                static_cast<int32_t>((tt / kbt) * 128), bar0 + 8 * b);
   };
   // the row path runs on threads 0..127; the column path on the next 128
   // (or on 0..127 when it is alone)
@@ -448,13 +439,14 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   __syncthreads();
   const int64_t t0 = blockIdx.x, t1 = blockIdx.x + gridDim.x;
   if (tid == 0) {
-    if (t0 < num_tiles) mbar_arrive_expect_tx(bar0, tile_bytes(t0));
-    if (t1 < num_tiles) mbar_arrive_expect_tx(bar0 + 8, tile_bytes(t1));
-  }
-  __syncthreads();
-  if (tid < 128) {
-    if (t0 < num_tiles) issue_row(t0, 0);
-    if (t1 < num_tiles) issue_row(t1, 1);
+    if (t0 < num_tiles) {
+      mbar_arrive_expect_tx(bar0, tile_bytes(t0));
+      issue_tile(t0, 0);
+    }
+    if (t1 < num_tiles) {
+      mbar_arrive_expect_tx(bar0 + 8, tile_bytes(t1));
+      issue_tile(t1, 1);
+    }
   }
 
   uint32_t it = 0;
@@ -473,14 +465,26 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     const int hh = ctid >> 6;
     if (ok) {
       if (row_role) {
-        const uint4* rp = reinterpret_cast<const uint4*>(tile + tid * kRcPitch);
+        // slot k (words 8k .. 8k+7) holds code chunk (k + tid) % 8, i.e. input
+        // chunks 2((k + tid) % 8) and +1; threads with (tid / 8) odd read the
+        // odd chunk of the pair first.  Each 16-byte read then spreads 32
+        // threads evenly over the 8 bank groups.
+        const uint8_t* rp = tile + tid * kRcPitch;
+        const int r8 = tid & 7, s8 = (tid >> 3) & 1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint4 q = rp[i];
-          w[4 * i] = q.x;
-          w[4 * i + 1] = q.y;
-          w[4 * i + 2] = q.z;
-          w[4 * i + 3] = q.w;
+        for (int k = 0; k < 8; ++k) {
+          const int kk = (k + r8) & 7;
+          const uint4 qa = *reinterpret_cast<const uint4*>(rp + (2 * kk + s8) * 16);
+          const uint4 qb = *reinterpret_cast<const uint4*>(rp + (2 * kk + 1 - s8) * 16);
+          const uint4 lo = s8 ? qb : qa, hi = s8 ? qa : qb;
+          w[8 * k] = lo.x;
+          w[8 * k + 1] = lo.y;
+          w[8 * k + 2] = lo.z;
+          w[8 * k + 3] = lo.w;
+          w[8 * k + 4] = hi.x;
+          w[8 * k + 5] = hi.y;
+          w[8 * k + 6] = hi.z;
+          w[8 * k + 7] = hi.w;
         }
       } else {
         const uint8_t* cp = tile + (hh * 64) * kRcPitch + p * 4;
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     // every thread has its values (buffer b is free), the staged code tiles
     // are free, or some wait failed
     if (__syncthreads_or(!ok)) break;
-    if (tid < 128 && tn < num_tiles) issue_row(tn, b);
+    if (tid == 0 && tn < num_tiles) issue_tile(tn, b);
 
     if (row_role) {
       // ---- 1x128 row group of row m
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
           c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
                             bf16hi_to_f32(bb) * inv);
         }
-        st[(i >> 1) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);
+        st[(((i >> 1) + tid) & 7) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);  // code chunk of slot i/2
       }
       fence_proxy_async_smem();
       asm volatile("bar.sync 3, 128;" ::: "memory");
