@@ -55,7 +55,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
-    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum", "mx"],
+    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum", "mx", "ceiling"],
                    help="all: the Fprop step plus the breakdown; else time one workload alone")
     p.add_argument("--no-breakdown", action="store_true", help="time the Fprop step only")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
@@ -539,11 +539,31 @@ def case_mx(args, f, torch, synth, pk, iters):
                 "roofline": hbm_roofline("quant_mx_kernel<bf16>", qbytes, ms_q, pk, "mx_act_16384x7168")}}
 
 
+def case_ceiling(args, f, torch, synth, pk, iters):
+    """Context, not the method: a library FP8 GEMM on the Fprop shape,
+    torch._scaled_mm (cuBLASLt) with one scale per tensor and no block
+    scaling or promotion, run and timed only.  None if unavailable."""
+    M, N, K = FPROP["M"], FPROP["N"], FPROP["K"]
+    try:
+        a = (torch.randn(M, K, device="cuda") * 0.5).to(torch.float8_e4m3fn)
+        b = (torch.randn(N, K, device="cuda") * 0.5).to(torch.float8_e4m3fn)
+        one = torch.ones((), device="cuda")
+        ms = _time(torch, lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16),
+                   iters)
+    except Exception as e:  # the library call itself is optional context
+        return {"torch._scaled_mm_TFLOP/s": None, "unavailable": str(e).splitlines()[0][:200]}
+    fl = 2.0 * M * N * K
+    return {"torch._scaled_mm_TFLOP/s": round(fl / ms / 1e9, 1), "ms": round(ms, 4),
+            "frac_of_burst_peak": round(fl / ms / 1e9 / fp8_peak(pk), 4),
+            "note": "per-tensor FP8 E4M3 GEMM (cuBLASLt), BF16 out, no block scales, no 128-K promotion"}
+
+
 CASES = {"act_quant_16384x7168": case_act, "wgrad_2048x7168x8192": case_wgrad,
          "moe_grouped_256x(7168->2048)": case_moe, "accum_precision_K4096": case_accum,
-         "mx_fprop_4096x18432x7168": case_mx}
+         "mx_fprop_4096x18432x7168": case_mx, "library_fp8_gemm_4096x18432x7168": case_ceiling}
 CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)",
-             "accum": "accum_precision_K4096", "mx": "mx_fprop_4096x18432x7168"}
+             "accum": "accum_precision_K4096", "mx": "mx_fprop_4096x18432x7168",
+             "ceiling": "library_fp8_gemm_4096x18432x7168"}
 
 
 def oracle_fprop_sample(xb, wb, R, C):
