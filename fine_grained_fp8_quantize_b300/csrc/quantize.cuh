@@ -367,9 +367,10 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
 
 // ---------------------------------------------------------------------------
 // Rows + transposed columns of BF16 activations in one pass, split by role.
-// Persistent, 256 threads, two 128 x 128 tiles in flight per CTA (bulk
-// copies, one 256-byte row per copy, into rows of a padded 272-byte pitch).
-//   warps 0-3  row path: thread r owns tile row r (16 x 16-byte reads); its
+// Persistent, 256 threads, two 128 x 128 tiles in flight per CTA, each
+// arriving as one dense TMA box (128 rows x 256 bytes).
+//   warps 0-3  row path: thread r owns tile row r (16 x 16-byte reads, in a
+//              rotated order that keeps them free of bank conflicts); its
 //              1x128 amax is a packed BF16 max over the row (no shuffles).
 //   warps 4-7  column path: thread (p, h) owns columns 2p, 2p+1 over the
 //              64 rows of half h (64 x 4-byte reads); the two halves meet in
