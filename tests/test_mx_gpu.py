@@ -148,6 +148,29 @@ def test_gemm_random_codes(f, M, N, K, out):
     check_gemm(C.reshape(-1), ex, ab, out == torch.bfloat16, "mx %dx%dx%d" % (M, N, K))
 
 
+def test_gemm_many_waves_ragged(f):
+    """More tiles than CTAs (the persistent loop's accumulator handoff between
+    tiles), a row tail and a half N-tile; checked on one full row per M-tile
+    and one full column per N-tile."""
+    M, N, K = 2100 * 2, 4608 + 128, 1152
+    rng = np.random.default_rng(77)
+    Aq, Bq = rand_codes(rng, (M, K)), rand_codes(rng, (N, K))
+    ea = rng.integers(117, 138, (M, K // 32)).astype(np.uint8)
+    eb = rng.integers(117, 138, (N, K // 32)).astype(np.uint8)
+    C = run_gemm(f, Aq, ea, Bq, eb, torch.float32)
+    mi, ni = sample_points(M, N)
+    ex, ab = oracle.mx_gemm_points(Aq, ea, Bq, eb, mi, ni)
+    check_gemm(C[mi, ni], ex, ab, False, "mx many waves")
+
+
+def test_quantize_fp32_ragged_rows(f):
+    x = (synth.matrix(41, 1, 333, 1280, 1.0, entry_frac=0.02, entry_scale=50.0, dtype=torch.float32) * 1e-3).cuda()
+    q, s = run_quant(f, x)
+    oq, oe = oracle.mx_quantize_rows(to_np(x))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(s, tile_scales(oe, 333, 1280))
+
+
 def test_gemm_zero_rows_is_noop(f):
     A = torch.empty(0, 256, dtype=torch.uint8, device="cuda")
     B = torch.zeros(128, 256, dtype=torch.uint8, device="cuda")
