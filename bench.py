@@ -49,13 +49,20 @@ FPROP_WORKLOAD = ("fprop 4096x18432x7168: quantize X 1x128 + quantize W 128x128 
                   "BF16 out")
 
 
+def fprop_config(world):
+    """The workload of one bench step (the same dict on both arms)."""
+    return {"workload": FPROP_WORKLOAD, "M": FPROP["M"], "N": FPROP["N"], "K": FPROP["K"],
+            "global_batch": FPROP["M"] * world, "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (323 MB BF16 per step), no flush"}
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
-    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "wgrad", "moe", "accum", "mx", "ceiling"],
+    p.add_argument("--case", default="all", choices=["all", "fprop", "act", "dgrad", "wgrad", "moe", "accum", "mx", "ceiling"],
                    help="all: the Fprop step plus the breakdown; else time one workload alone")
     p.add_argument("--no-breakdown", action="store_true", help="time the Fprop step only")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
@@ -180,6 +187,126 @@ class ClockSampler:
                 "samples": len(mhz), "power_w_median": float(np.median(watts))}
 
 
+class _CtypesNvml:
+    """The few read-only NVML queries NvmlClocks makes, through ctypes on the
+    driver's libnvidia-ml.so.1 (for hosts without the pynvml module)."""
+
+    NVML_CLOCK_SM = 1
+    nvmlClocksEventReasonSwPowerCap = 0x4
+    nvmlClocksEventReasonHwSlowdown = 0x8
+    nvmlClocksEventReasonSwThermalSlowdown = 0x20
+    nvmlClocksEventReasonHwThermalSlowdown = 0x40
+    nvmlClocksEventReasonHwPowerBrakeSlowdown = 0x80
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.L = None
+
+    def _ok(self, r, what):
+        if r != 0:
+            raise RuntimeError("%s returned %d" % (what, r))
+
+    def nvmlInit(self):
+        self.L = self.c.CDLL("libnvidia-ml.so.1")
+        self._ok(self.L.nvmlInit_v2(), "nvmlInit_v2")
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.c.c_void_p()
+        self._ok(self.L.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.c.byref(h)), "GetHandleByPciBusId")
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self.c.c_void_p()
+        self._ok(self.L.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(i), self.c.byref(h)), "GetHandleByIndex")
+        return h
+
+    def _uint(self, fn, h, *args):
+        v = self.c.c_uint()
+        self._ok(fn(h, *args, self.c.byref(v)), fn.__name__)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, which):
+        return self._uint(self.L.nvmlDeviceGetClockInfo, h, self.c.c_int(which))
+
+    def nvmlDeviceGetMaxClockInfo(self, h, which):
+        return self._uint(self.L.nvmlDeviceGetMaxClockInfo, h, self.c.c_int(which))
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint(self.L.nvmlDeviceGetPowerUsage, h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        self._ok(self.L.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.c.byref(v)), "GetCurrentClocksReasons")
+        return v.value
+
+
+class NvmlClocks:
+    """Read-only NVML samples (SM clock, max SM clock, power, clock-event
+    reasons) polled by the host while the GPU runs the timed region.  This
+    covers timed regions shorter than nvidia-smi's sampling period."""
+
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
+
+    def __init__(self, torch, index):
+        self.nv = self.h = None
+        self.samples = []
+        self.error = None
+        try:
+            import pynvml as nv
+        except ImportError:
+            nv = _CtypesNvml()  # the driver's libnvidia-ml through ctypes
+        try:
+            nv.nvmlInit()
+            self.nv = nv
+        except Exception as e:  # no NVML: the nvidia-smi samples stand alone
+            self.error = "nvmlInit: %s" % e
+            return
+        try:
+            p = torch.cuda.get_device_properties(index)
+            bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            self.h = nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception as e:
+            self.error = "by PCI bus id: %s" % e
+        if self.h is None:
+            try:
+                self.h = nv.nvmlDeviceGetHandleByIndex(index)
+            except Exception as e:
+                self.error = (self.error or "") + "; by index: %s" % e
+
+    def sample(self):
+        if self.h is None:
+            return
+        nv = self.nv
+        try:
+            mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+            mx = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            w = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+            r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        except Exception as e:
+            self.error = "query: %s" % e
+            return
+        self.samples.append((mhz, mx, w, r))
+
+    def summary(self):
+        if not self.samples:
+            return None
+        nv = self.nv
+        reasons = set()
+        for _, _, _, r in self.samples:
+            for name, attr in self.REASONS:
+                if r & getattr(nv, attr, 0):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([s[0] for s in self.samples])),
+                "sm_max_mhz": float(max(s[1] for s in self.samples)), "reasons": sorted(reasons),
+                "samples": len(self.samples), "power_w_median": float(np.median([s[2] for s in self.samples])),
+                "source": "NVML polled by the host while the GPU ran the timed region"}
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
@@ -188,7 +315,7 @@ def fp8_peak(pk):
     return pk["bf16"] * FP8_PER_BF16
 
 
-def tensor_roofline(kernel, flops, ms, pk, workload, sustained=False):
+def tensor_roofline(kernel, flops, ms, pk, workload, sustained=False, note=True):
     """Dense FP8 roofline of one kernel.  `sustained`: the kernel was timed
     inside a long run of back-to-back steps (seconds under the power cap), so
     the denominator is the measured sustained BF16 figure x 2; otherwise the
@@ -206,14 +333,16 @@ def tensor_roofline(kernel, flops, ms, pk, workload, sustained=False):
                          % (pk["src"], "sustained" if sustained else "burst",
                             pk["bf16_sus"] if sustained else pk["bf16"], pk["src"], burst, sus, tf / 4500.0),
             "ms_per_launch": round(ms, 5), "flops_per_launch": flops,
-            "traffic": recorded_traffic(kernel.split("<")[0], workload)}
+            "traffic": recorded_traffic(kernel.split("<")[0], workload)} if note else {
+        "kernel": kernel, "bound": "tensor", "achieved": round(tf, 1), "peak": round(burst, 1), "unit": "TFLOP/s",
+        "frac": round(tf / burst, 4), "peak_kind": "burst", "ms_per_launch": round(ms, 5),
+        "flops_per_launch": flops, "traffic": recorded_traffic(kernel.split("<")[0], workload)}
 
 
 def hbm_roofline(kernel, nbytes, ms, pk, workload):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-            "frac": round(gbs / pk["hbm"], 4),
-            "peak_note": "%s STREAM-style copy; vs 8 TB/s nominal = %.4f" % (pk["src"], gbs / 8000.0),
+            "frac": round(gbs / pk["hbm"], 4), "frac_vs_8TBs_nominal": round(gbs / 8000.0, 4),
             "ms_per_launch": round(ms, 5), "bytes_per_launch": nbytes,
             "traffic": recorded_traffic(kernel.split("<")[0], workload)}
 
@@ -268,20 +397,38 @@ def run_timed(torch, stream, step, steps, warmup, dist=None):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device())
+    nvml = NvmlClocks(torch, torch.cuda.current_device())
     with sampler:
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         sampler.mark_start()
+        h0 = time.perf_counter()
         t0.record(stream)
         for _ in range(steps):
             step(True)
         t1.record(stream)
+        host_ms = (time.perf_counter() - h0) * 1e3
+        # the launches are queued: sample the clocks until the GPU is done
+        while not t1.query():
+            nvml.sample()
+            time.sleep(0.0002)
         torch.cuda.synchronize()
         sampler.mark_stop()
         if dist:
             dist.barrier()
-    return t0.elapsed_time(t1), sampler.summary()
+    clocks = sampler.summary()
+    clocks["host_enqueue_ms_per_step"] = round(host_ms / max(1, steps), 4)
+    polled = nvml.summary()
+    if polled is not None and (clocks.get("samples", 0) < 5 or clocks.get("sm_mhz") is None):
+        polled["nvidia_smi_samples"] = clocks.get("samples", 0)
+        polled["host_enqueue_ms_per_step"] = clocks["host_enqueue_ms_per_step"]
+        clocks = polled
+    elif polled is None:
+        clocks["nvml"] = "no samples: the GPU finished before the host had queued every step" \
+            if nvml.h is not None and nvml.error is None else "NVML unavailable (%s)" % nvml.error
+
+    return t0.elapsed_time(t1), clocks
 
 
 def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
@@ -296,32 +443,41 @@ def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
     sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device="cuda")
     Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     tg = Timed(torch, args.steps)
+    tx = Timed(torch, args.steps)
+    tw = Timed(torch, args.steps)
 
     def step(timed):
-        f.fp8q_quantize_act(X, qx, sx)
-        f.fp8q_quantize_weight(W, qw, sw)
         if timed:
+            tx(stream, lambda: f.fp8q_quantize_act(X, qx, sx))
+            tw(stream, lambda: f.fp8q_quantize_weight(W, qw, sw))
             tg(stream, lambda: f.fp8q_gemm(qx, sx, qw, sw, Y))
         else:
+            f.fp8q_quantize_act(X, qx, sx)
+            f.fp8q_quantize_weight(W, qw, sw)
             f.fp8q_gemm(qx, sx, qw, sw, Y)
 
     ms, clocks = run_timed(torch, stream, step, args.steps, args.warmup, dist)
     check_status(f, "after the fprop timing")
     ms = max_over_ranks(torch, ms, dist, "cuda")
     value = replica_value(world, flops, args.steps, ms)
+    xbytes = M * K * 2 + M * K + (K // 128) * M * 4
+    wbytes = N * K * 2 + N * K + (N // 128) * (K // 128) * 4
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
         "data": "synthetic (seeded SplitMix64 + Box-Muller; X N(0,1) with 0.1% x1e3, W N(0,0.02^2))",
-        "config": {"workload": FPROP_WORKLOAD, "M": M, "N": N, "K": K, "global_batch": M * world,
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": "inputs larger than L2 (323 MB BF16 per step), no flush"},
+        "config": fprop_config(world),
         # timed inside the whole run of back-to-back steps: when that run
         # lasts half a second or more (under the power cap) the sustained
         # peak is the denominator, else the burst peak
         "roofline": tensor_roofline("gemm_kernel<bf16 out, 128x128 B scales>", flops, tg.mean_ms(), pk,
                                     "fprop_4096x18432x7168", sustained=ms >= 500.0),
+        "step_kernels": {
+            "quant_x_rows_4096x7168": hbm_roofline("quant_rows_kernel<bf16>", xbytes, tx.mean_ms(), pk,
+                                                   "x_rows_4096x7168"),
+            "quant_w_blocks_18432x7168": hbm_roofline("quant_pipe_kernel<blk>", wbytes, tw.mean_ms(), pk,
+                                                      "w_blocks_18432x7168")},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -417,13 +573,49 @@ def case_wgrad(args, f, torch, synth, pk, iters):
     ms_all = _time(torch, lambda: (f.fp8q_quantize_act(dY, None, None, qdy, sdy),
                                    f.fp8q_quantize_act(Xw, None, None, qx, sx),
                                    f.fp8q_gemm_ws(qdy, sdy, qx, sx, dW, 1, ws)), iters)
+    ms_qdy = _time(torch, lambda: f.fp8q_quantize_act(dY, None, None, qdy, sdy), iters)
+    ms_qx = _time(torch, lambda: f.fp8q_quantize_act(Xw, None, None, qx, sx), iters)
+    qb_dy = Tt * Do * 2 + Tt * Do + (Tt // 128) * Do * 4
+    qb_x = Tt * Di * 2 + Tt * Di + (Tt // 128) * Di * 4
     check_status(f, "after wgrad")
     fl = 2.0 * Do * Di * Tt
     return {"gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1),
             "gemm_ms_without_streamk": round(ms_dp, 4),
             "step_ms": round(ms_all, 4), "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
             "roofline": tensor_roofline("gemm_kernel<f32 out, per-column B scales, stream-K>", fl, ms_g, pk,
-                                        "wgrad_2048x7168x8192")}
+                                        "wgrad_2048x7168x8192", note=False),
+            "quant_cols_dY_8192x2048": hbm_roofline("quant_pipe_kernel<col>", qb_dy, ms_qdy, pk, "cols_8192x2048"),
+            "quant_cols_X_8192x7168": hbm_roofline("quant_pipe_kernel<col>", qb_x, ms_qx, pk, "cols_8192x7168")}
+
+
+def case_dgrad(args, f, torch, synth, pk, iters):
+    """Dgrad dX = dY . W: dY BF16 4096x18432 in 1x128 groups, the Fprop
+    weight's transposed 128x128-block codes as B (M 4096, N 7168, K 18432),
+    BF16 out."""
+    M, N, K = FPROP["M"], FPROP["K"], FPROP["N"]
+    dY = synth.matrix(5, 1, M, K, 1e-3, entry_frac=5e-3, entry_scale=50.0, device="cuda")
+    _, W = synth.fprop_inputs(device="cuda", M=128)
+    qdy = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    sdy = torch.empty(K // 128, M, dtype=torch.float32, device="cuda")
+    qwt = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    swt = torch.empty(N // 128, K // 128, dtype=torch.float32, device="cuda")
+    dX = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    f.fp8q_quantize_act(dY, qdy, sdy)
+    f.fp8q_quantize_weight_ex(W, None, None, qwt, swt)
+    ms_g = _time(torch, lambda: f.fp8q_gemm(qdy, sdy, qwt, swt, dX), iters)
+    ms_all = _time(torch, lambda: (f.fp8q_quantize_act(dY, qdy, sdy),
+                                   f.fp8q_quantize_weight_ex(W, None, None, qwt, swt),
+                                   f.fp8q_gemm(qdy, sdy, qwt, swt, dX)), iters)
+    ms_wt = _time(torch, lambda: f.fp8q_quantize_weight_ex(W, None, None, qwt, swt), iters)
+    check_status(f, "after dgrad")
+    fl = 2.0 * M * N * K
+    wtbytes = K * N * 2 + K * N + (K // 128) * (N // 128) * 4
+    return {"gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
+            "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
+            "roofline": tensor_roofline("gemm_kernel<bf16 out, 128x128 B scales>", fl, ms_g, pk,
+                                        "dgrad_4096x7168x18432", note=False),
+            "quant_w_transposed_18432x7168": hbm_roofline("quant_pipe_kernel<blkT>", wtbytes, ms_wt, pk,
+                                                          "w_blocksT_18432x7168")}
 
 
 def case_moe(args, f, torch, synth, pk, iters):
@@ -457,7 +649,8 @@ def case_moe(args, f, torch, synth, pk, iters):
             "gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
             "bound": "tensor" if t_comp > t_mem else "hbm",
             "roofline_frac": round(max(t_comp, t_mem) / (ms_g * 1e-3), 4), "min_bytes": gbytes,
-            "roofline": tensor_roofline("gemm_kernel<bf16 out, grouped>", fl, ms_g, pk, "moe_256x2048x7168")}
+            "roofline": tensor_roofline("gemm_kernel<bf16 out, grouped>", fl, ms_g, pk, "moe_256x2048x7168",
+                                        note=False)}
 
 
 def case_accum(args, f, torch, synth, pk, iters):
@@ -533,7 +726,8 @@ def case_mx(args, f, torch, synth, pk, iters):
     qbytes = T * H * 2 + T * H + f.fp8q_mx_scale_bytes(T, H)
     return {"gemm_ms": round(ms_g, 4), "gemm_TFLOP/s": round(fl / ms_g / 1e9, 1), "step_ms": round(ms_all, 4),
             "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
-            "roofline": tensor_roofline("gemm_mx_kernel<bf16 out>", fl, ms_g, pk, "mx_fprop_4096x18432x7168"),
+            "roofline": tensor_roofline("gemm_mx_kernel<bf16 out>", fl, ms_g, pk, "mx_fprop_4096x18432x7168",
+                                        note=False),
             "act_quant_16384x7168": {
                 "ms": round(ms_q, 4), "GB/s": round(qbytes / (ms_q * 1e-3) / 1e9, 1), "bytes": qbytes,
                 "roofline": hbm_roofline("quant_mx_kernel<bf16>", qbytes, ms_q, pk, "mx_act_16384x7168")}}
@@ -558,18 +752,20 @@ def case_ceiling(args, f, torch, synth, pk, iters):
             "note": "per-tensor FP8 E4M3 GEMM (cuBLASLt), BF16 out, no block scales, no 128-K promotion"}
 
 
-CASES = {"act_quant_16384x7168": case_act, "wgrad_2048x7168x8192": case_wgrad,
+CASES = {"act_quant_16384x7168": case_act, "dgrad_4096x7168x18432": case_dgrad, "wgrad_2048x7168x8192": case_wgrad,
          "moe_grouped_256x(7168->2048)": case_moe, "accum_precision_K4096": case_accum,
          "mx_fprop_4096x18432x7168": case_mx, "library_fp8_gemm_4096x18432x7168": case_ceiling}
-CASE_KEYS = {"act": "act_quant_16384x7168", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)",
+CASE_KEYS = {"act": "act_quant_16384x7168", "dgrad": "dgrad_4096x7168x18432", "wgrad": "wgrad_2048x7168x8192", "moe": "moe_grouped_256x(7168->2048)",
              "accum": "accum_precision_K4096", "mx": "mx_fprop_4096x18432x7168",
              "ceiling": "library_fp8_gemm_4096x18432x7168"}
 
 
-def oracle_fprop_sample(xb, wb, R, C):
+def oracle_fprop_sample(xb, wb, R, C, keep=None):
     """The CPU oracle as it stands on a slice of the Fprop step: quantize R
     rows of X (1x128), quantize the first C rows of W (C/128 row-blocks of
-    128x128 blocks), compute the R x C outputs.  -> (seconds, FLOPs)."""
+    128x128 blocks), compute the R x C outputs.  -> (seconds, FLOPs); with
+    ``keep`` (a dict) the outputs (exact, sum|ab|, pages order) are left in
+    it."""
     import oracle
     K = FPROP["K"]
     t = time.perf_counter()
@@ -577,8 +773,11 @@ def oracle_fprop_sample(xb, wb, R, C):
     qw, sw = oracle.quantize_weight(wb[:C])
     mi = np.repeat(np.arange(R), C)
     ni = np.tile(np.arange(C), R)
-    oracle.gemm_points(qx, sx, qw, sw, mi, ni)
-    return time.perf_counter() - t, 2.0 * R * C * K
+    res = oracle.gemm_points(qx, sx, qw, sw, mi, ni)
+    dt = time.perf_counter() - t
+    if keep is not None:
+        keep.update(exact=res[0], absref=res[1], pages=res[2], mi=mi, ni=ni)
+    return dt, 2.0 * R * C * K
 
 
 def _scale_sample(R, C, factor):
@@ -606,15 +805,41 @@ def oracle_sample_size(xb, wb, seconds):
     return _scale_sample(R, C, seconds / max(dt, 1e-6))
 
 
-def cpu_baseline_fprop(X, W, budget_s):
+def cpu_baseline_fprop(f, torch, X, W, budget_s):
+    """The oracle on a bounded sample of the Fprop step, on every host core
+    and on one; then, from the same sample, the tensor-core accumulation
+    diagnostic: the GPU GEMM with FP32 output against the oracle's literal
+    FP32 procedure of the pages (|C_gpu - C_pages| / sum|ab|)."""
     import oracle
     import synth
     xb, wb = synth.bf16_bits(X), synth.bf16_bits(W)
+    cores = oracle.num_threads()
     R, C = oracle_sample_size(xb, wb, budget_s)
-    dt, fl = oracle_fprop_sample(xb, wb, R, C)
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d of 4096 rows x %d of 18432 columns of the fprop step: quantize those rows of X and "
-                      "those %d rows of W, compute the %dx%d outputs; %.1f s" % (R, C, C, R, C, dt)}
+    keep = {}
+    dt, fl = oracle_fprop_sample(xb, wb, R, C, keep)
+    out = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": "%d of 4096 rows x %d of 18432 columns of the fprop step: quantize those rows of X and "
+                     "those %d rows of W, compute the %dx%d outputs; %.1f s" % (R, C, C, R, C, dt)}
+    oracle.set_num_threads(1)
+    try:
+        R1, C1 = oracle_sample_size(xb, wb, budget_s / 2)
+        dt1, fl1 = oracle_fprop_sample(xb, wb, R1, C1)
+    finally:
+        oracle.set_num_threads(cores)
+    out["one_core"] = {"value": round(fl1 / dt1 / 1e12, 6), "cores": 1,
+                       "sample": "%d rows x %d columns, %.1f s" % (R1, C1, dt1)}
+    # the same sampled outputs from the GPU with FP32 output
+    qx, sx, _, _ = f.quantize_act(X[:R])
+    qw, sw = f.quantize_weight(W[:C])
+    Cg = f.gemm(qx, sx, qw, sw, out_dtype=torch.float32).double().cpu().numpy()
+    g = Cg[keep["mi"], keep["ni"]]
+    ab = keep["absref"]
+    out["accum_diag"] = {
+        "max_abs_gpu_minus_pages_over_sum_abs": float((np.abs(g - keep["pages"]) / ab).max()),
+        "max_abs_gpu_minus_exact_over_sum_abs": float((np.abs(g - keep["exact"]) / ab).max()),
+        "max_abs_pages_minus_exact_over_sum_abs": float((np.abs(keep["pages"] - keep["exact"]) / ab).max()),
+        "outputs": int(g.size), "K": FPROP["K"]}
+    return out
 
 
 def gpu_arm(args, rank, world, dist):
@@ -637,8 +862,49 @@ def gpu_arm(args, rank, world, dist):
     if rank == 0 and not args.no_breakdown:
         out["breakdown"] = {k: fn(args, f, torch, synth, pk, iters) for k, fn in CASES.items()}
     if rank == 0 and not args.no_cpu:
-        out["cpu_baseline"] = cpu_baseline_fprop(X, W, args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline_fprop(f, torch, X, W, args.cpu_budget)
+    out["summary"] = summary(out)
     return out
+
+
+def summary(out):
+    """A compact digest of every kernel's roofline, emitted as the line's last
+    key so that it survives a log that keeps only the line's tail."""
+    def t(r):
+        d = {"TFLOP/s": r["achieved"], "frac": r["frac"], "peak": r["peak"]}
+        if r.get("traffic"):
+            d["dram_MB"] = round(r["traffic"] / 1e6, 1)
+        return d
+
+    def h(r):
+        d = {"GB/s": r["achieved"], "frac": r["frac"]}
+        if r.get("traffic"):
+            d["dram_over_alg"] = round(r["traffic"] / r["bytes_per_launch"], 3)
+        return d
+
+    sm = {"step_TFLOP/s": out["value"], "fprop_gemm": t(out["roofline"])}
+    for k, r in out.get("step_kernels", {}).items():
+        sm[k] = h(r)
+    bd = out.get("breakdown", {})
+    if "act_quant_16384x7168" in bd:
+        sm["quant_act_rows_cols_16384x7168"] = h(bd["act_quant_16384x7168"]["roofline"])
+    if "dgrad_4096x7168x18432" in bd:
+        sm["dgrad_gemm"] = t(bd["dgrad_4096x7168x18432"]["roofline"])
+        sm["quant_w_transposed"] = h(bd["dgrad_4096x7168x18432"]["quant_w_transposed_18432x7168"])
+    if "wgrad_2048x7168x8192" in bd:
+        w = bd["wgrad_2048x7168x8192"]
+        sm["wgrad_gemm"] = t(w["roofline"])
+        sm["quant_cols_dY"] = h(w["quant_cols_dY_8192x2048"])
+        sm["quant_cols_X"] = h(w["quant_cols_X_8192x7168"])
+    if "moe_grouped_256x(7168->2048)" in bd:
+        sm["moe_gemm"] = t(bd["moe_grouped_256x(7168->2048)"]["roofline"])
+    if "mx_fprop_4096x18432x7168" in bd:
+        mx = bd["mx_fprop_4096x18432x7168"]
+        sm["mx_gemm"] = t(mx["roofline"])
+        sm["mx_quant_act"] = h(mx["act_quant_16384x7168"]["roofline"])
+    c = out.get("clocks") or {}
+    sm["sm_mhz"] = c.get("sm_mhz")
+    return sm
 
 
 # ---------------------------------------------------------------------------
@@ -667,7 +933,7 @@ def reference_arm(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64 exact / f32 promotion order (CPU)", "data": "synthetic",
-            "config": {"workload": FPROP_WORKLOAD + " (bounded sample per step)", "M": M, "N": N, "K": K},
+            "config": fprop_config(args.gpus),
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

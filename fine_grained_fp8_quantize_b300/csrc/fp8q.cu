@@ -331,6 +331,7 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   a.row_offsets = row_offsets;
   a.E = grouped ? E : 1;
   a.streamk = 0;
+  a.sk_tile0 = 0;
   a.ws = nullptr;
   a.flags = nullptr;
   a.epoch = 0;
@@ -353,6 +354,9 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
         kb_total < (int64_t(1) << 62) / di.sms) {
       grid = di.sms;
       a.streamk = 1;
+      // whole-tile waves first, the last full wave plus the remainder
+      // balanced by stream-K
+      a.sk_tile0 = static_cast<int>(waves >= 2 ? (waves - 2) * di.sms : 0);
       a.flags = static_cast<uint32_t*>(workspace);
       a.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) +
                                        ((static_cast<size_t>(di.sms) * 4 + 255) & ~size_t(255)));

@@ -82,12 +82,15 @@ struct GemmArgs {
   int tiles_n;
   const int32_t* row_offsets;  // grouped [E+1]
   int E;
-  // stream-K (dense only, kernel variant kStreamK): each CTA takes an equal
-  // share of the tile-major sequence of all tiles' K-blocks; a tile split
-  // between CTAs is finished by the CTA holding its first K-blocks, which
-  // adds the other CTAs' FP32 partial tiles (ws, slot = CTA index) once
-  // their flags carry this call's epoch.
+  // stream-K (dense only, kernel variant kStreamK): tiles below sk_tile0 are
+  // whole tiles striped over the CTAs (data-parallel waves, which keep
+  // concurrently running CTAs on neighbouring tiles); each CTA then takes
+  // an equal share of the tile-major sequence of the remaining tiles'
+  // K-blocks.  A tile split between CTAs is finished by the CTA holding its
+  // first K-blocks, which adds the other CTAs' FP32 partial tiles (ws, slot
+  // = CTA index) once their flags carry this call's epoch.
   int streamk;
+  int sk_tile0;
   float4* ws;        // [gridDim.x][2 halves][32 column quads][128 rows] float4
   uint32_t* flags;   // [gridDim.x], zero between calls
   uint32_t epoch;    // nonzero, distinct from the previous call's
@@ -97,6 +100,43 @@ struct GemmArgs {
 // K-blocks (CTA c takes [begin(c), begin(c+1))).
 __device__ __forceinline__ int64_t streamk_begin(int64_t total, int64_t cta, int64_t grid) {
   return total * cta / grid;
+}
+
+// This CTA's work as segments (tile t, K-blocks [lo, hi)): the tiles
+// t = blockIdx.x + i * gridDim.x below the stream-K start (whole tiles),
+// then, in the stream-K variant, its equal share of the K-blocks of the
+// tiles from a.sk_tile0 on.  f(t, lo, hi) returns false to stop.
+template <bool kStreamK, typename F>
+__device__ __forceinline__ void for_each_segment(const GemmArgs& a, int num_tiles, int64_t KB, F&& f) {
+  const int dp_end = kStreamK ? a.sk_tile0 : num_tiles;
+  for (int t = blockIdx.x; t < dp_end; t += gridDim.x)
+    if (!f(t, int64_t(0), KB)) return;
+  if constexpr (kStreamK) {
+    const int64_t all = static_cast<int64_t>(num_tiles - a.sk_tile0) * KB;
+    const int64_t e = streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x);
+    for (int64_t it = streamk_begin(all, blockIdx.x, gridDim.x); it < e;) {
+      const int tr = static_cast<int>(it / KB);
+      const int64_t lo = it - static_cast<int64_t>(tr) * KB;
+      const int64_t hi = e - static_cast<int64_t>(tr) * KB < KB ? e - static_cast<int64_t>(tr) * KB : KB;
+      if (!f(a.sk_tile0 + tr, lo, hi)) return;
+      it += hi - lo;
+    }
+  }
+}
+
+// K-blocks of all of this CTA's segments.
+template <bool kStreamK>
+__device__ __forceinline__ uint64_t cta_kblocks(const GemmArgs& a, int num_tiles, int64_t KB) {
+  const int dp_end = kStreamK ? a.sk_tile0 : num_tiles;
+  const int64_t local_tiles =
+      static_cast<int>(blockIdx.x) < dp_end ? (dp_end - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  uint64_t total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
+  if constexpr (kStreamK) {
+    const int64_t all = static_cast<int64_t>(num_tiles - a.sk_tile0) * KB;
+    total += static_cast<uint64_t>(streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x) -
+                                   streamk_begin(all, blockIdx.x, gridDim.x));
+  }
+  return total;
 }
 
 struct TileInfo {
@@ -266,19 +306,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       };
-      if constexpr (!kStreamK) {
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) load_tile(t, 0, KB);
-      } else {
-        const int64_t all = static_cast<int64_t>(num_tiles) * KB;
-        const int64_t e = streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x);
-        for (int64_t it = streamk_begin(all, blockIdx.x, gridDim.x); ok && it < e;) {
-          const int t = static_cast<int>(it / KB);
-          const int64_t lo = it - static_cast<int64_t>(t) * KB;
-          const int64_t hi = e - static_cast<int64_t>(t) * KB < KB ? e - static_cast<int64_t>(t) * KB : KB;
-          load_tile(t, lo, hi);
-          it += hi - lo;
-        }
-      }
+      for_each_segment<kStreamK>(args, num_tiles, KB, [&](int t, int64_t lo, int64_t hi) {
+        load_tile(t, lo, hi);
+        return ok;
+      });
       if (!ok && lane == 0) {
         // drain: wait (bounded) for the copies still in flight
         for (uint32_t i = 0; i < kStages && i < issued; ++i) {
@@ -303,16 +334,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // warp-uniform; one elected lane issues the MMAs and the commits.
     // (Issued from lane 0 alone, the same loop cost the issuing thread about
     // twice as long per K-block, longer than the K-block's MMAs take.)
-    uint64_t total;  // K-blocks of this CTA
-    if constexpr (kStreamK) {
-      const int64_t all = static_cast<int64_t>(num_tiles) * KB;
-      total = static_cast<uint64_t>(streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x) -
-                                    streamk_begin(all, blockIdx.x, gridDim.x));
-    } else {
-      const int64_t local_tiles =
-          blockIdx.x < static_cast<unsigned>(num_tiles) ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-      total = static_cast<uint64_t>(local_tiles) * static_cast<uint64_t>(KB);
-    }
+    const uint64_t total = cta_kblocks<kStreamK>(args, num_tiles, KB);  // K-blocks of this CTA
     bool ok = true, any = false;
     for (uint64_t g = 0; g < total; ++g) {
       const uint32_t stage = static_cast<uint32_t>(g % kStages);
@@ -455,8 +477,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (kb_hi < KB) {
           // this CTA holds the first K-blocks of a split tile: add the
           // partials of the CTAs holding the rest, in CTA order
-          const int64_t all = static_cast<int64_t>(num_tiles) * KB;
-          const int64_t tile_end = static_cast<int64_t>(t + 1) * KB;
+          const int64_t all = static_cast<int64_t>(num_tiles - args.sk_tile0) * KB;
+          const int64_t tile_end = static_cast<int64_t>(t - args.sk_tile0 + 1) * KB;
           for (int64_t j = static_cast<int64_t>(blockIdx.x) + 1; j < gridDim.x; ++j) {
             const int64_t bj = streamk_begin(all, j, gridDim.x);
             if (bj >= tile_end) break;
@@ -547,19 +569,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     };
-    if constexpr (!kStreamK) {
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) tile_work(t, 0, KB);
-    } else {
-      const int64_t all = static_cast<int64_t>(num_tiles) * KB;
-      const int64_t e = streamk_begin(all, static_cast<int64_t>(blockIdx.x) + 1, gridDim.x);
-      for (int64_t it = streamk_begin(all, blockIdx.x, gridDim.x); ok && it < e;) {
-        const int t = static_cast<int>(it / KB);
-        const int64_t lo = it - static_cast<int64_t>(t) * KB;
-        const int64_t hi = e - static_cast<int64_t>(t) * KB < KB ? e - static_cast<int64_t>(t) * KB : KB;
-        tile_work(t, lo, hi);
-        it += hi - lo;
-      }
-    }
+    for_each_segment<kStreamK>(args, num_tiles, KB, [&](int t, int64_t lo, int64_t hi) {
+      tile_work(t, lo, hi);
+      return ok;
+    });
     // every TMA store of this warp has completed before the CTA exits
     if (lane == 0) bulk_wait_all();
     __syncwarp();

@@ -153,6 +153,13 @@ FP8Q_API int fp8q_quantize_weight_ex(const void *w, int in_dtype, int64_t N, int
 
 /*
  * fp8q_gemm -- block-scaled FP8 GEMM with FP32 promotion every 128 K.
+ * Passages: the tensor cores accumulate each 128-element K interval, the
+ * partial is then copied to FP32 registers on the CUDA cores and added at
+ * full precision ("Eliminate Deepseek Ai News For Good", the MMA-precision
+ * passage; inprokorea.com page, the accumulation-interval passage); the
+ * per-group scales are multiplied in at that promotion ("Is aI Hitting a
+ * Wall?", the dequantization passage); FP8 inputs, BF16 or FP32 output
+ * ("Deepseek Ai News Expert Interview", the GEMM input/output passage).
  *   Aq  [M][K] E4M3 codes, K contiguous (1x128-quantized rows).
  *   sA  [K/128][M] scales of A.
  *   Bq  [N][K] E4M3 codes, K contiguous (a weight in Linear layout).
@@ -169,7 +176,12 @@ FP8Q_API int fp8q_gemm(const uint8_t *Aq, const float *sA, const uint8_t *Bq, co
               fp8q_stream_t stream);
 
 /*
- * fp8q_gemm_ex -- fp8q_gemm with a choice of B-scale granularity along N:
+ * fp8q_gemm_ex -- fp8q_gemm with a choice of B-scale granularity along N.
+ * Passages: Wgrad runs in FP8 like Fprop and Dgrad (dssusan.co.kr page, the
+ * Figure 6 passage; "Is aI Hitting a Wall?", the FP8 Wgrad sentence), whose
+ * operands are grouped along the token dimension, so B's scale varies per
+ * column; the promotion is fp8q_gemm's.
+ *
  *   sb_gran_n == 128: sB is [N/128][K/128] (as fp8q_gemm);
  *   sb_gran_n == 1:   sB is [K/128][N], one scale per column n and K-block,
  *                     the layout of fp8q_quantize_act's s_col.  This is
@@ -227,7 +239,9 @@ FP8Q_API int fp8q_gemm_ws(const uint8_t *Aq, const float *sA, const uint8_t *Bq,
  *    FP8Q_ERR_WORKSPACE.
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    stream capture.  The cached address belongs to the device's current
+ *    primary context: do not call this entry point again after
+ *    cudaDeviceReset() on that device in the same process.
  *  - Every call shares the one array and leaves its contents for the next;
  *    each call first clears the flag words on its stream (a small memset).
  *    Calls whose kernels overlap on the GPU race on the array: keep them on
@@ -242,6 +256,11 @@ FP8Q_API int fp8q_gemm_ws_static(const uint8_t *Aq, const float *sA, const uint8
 /*
  * fp8q_grouped_gemm -- MoE grouped block-scaled FP8 GEMM over E experts with
  * ragged rows (no token dropping).
+ * Passages: activations are quantized to FP8 before the dispatch and each
+ * expert's up-projection consumes them in FP8 ("Eliminate Deepseek Ai News
+ * For Good", the dispatch passage); no routed token is dropped
+ * (inprokorea.com page, the no-token-dropping sentence); each expert's GEMM
+ * promotes every 128 K as fp8q_gemm does.
  *   Aq           [total_rows][K] codes of the dispatched (expert-grouped) rows.
  *   sA           [K/128][total_rows] their scales.
  *   Bq           [E][N][K] expert weights' codes;  sB [E][N/128][K/128].

@@ -52,6 +52,7 @@ def lib():
         L.oracle_grouped_gemm_points.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                                  P, P, I64, P, P, P]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_mx_shared_exp.restype = ctypes.c_int
         L.oracle_mx_shared_exp.argtypes = [ctypes.c_float]
         L.oracle_mx_quantize_rows.argtypes = [P, I32, I64, I64, P, P]
@@ -80,6 +81,11 @@ def _xin(x):
 
 def num_threads():
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n):
+    """Run later oracle calls on ``n`` OpenMP threads (timing only)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def e4m3_decode(codes):

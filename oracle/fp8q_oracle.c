@@ -511,3 +511,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Set the number of OpenMP threads later oracle calls run on (host
+ * scheduling only; the arithmetic and its order per output are unchanged). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}

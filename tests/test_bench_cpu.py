@@ -87,3 +87,23 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"].startswith(bench.FPROP_WORKLOAD)
+    # the same workload dict as the GPU arm's line
+    assert d["config"] == bench.fprop_config(1)
+
+
+def test_summary_is_compact_and_last():
+    r = bench.tensor_roofline("gemm_kernel<x>", 1.5e12, 1.0, PK, "no_such_workload")
+    q = bench.hbm_roofline("quant_rows_kernel<x>", 3.0e9, 1.0, PK, "no_such_workload")
+    out = {"value": 1.0, "roofline": r, "step_kernels": {"quant_x_rows_4096x7168": q},
+           "breakdown": {"act_quant_16384x7168": {"roofline": q},
+                         "wgrad_2048x7168x8192": {"roofline": r, "quant_cols_dY_8192x2048": q,
+                                                  "quant_cols_X_8192x7168": q}},
+           "clocks": {"sm_mhz": 2032.0}}
+    out["summary"] = bench.summary(out)
+    line = json.dumps(out)
+    tail = line[-1500:]
+    # every kernel's fraction sits inside the last 1500 characters
+    for key in ("fprop_gemm", "quant_x_rows_4096x7168", "quant_act_rows_cols_16384x7168", "wgrad_gemm",
+                "quant_cols_dY", "quant_cols_X"):
+        assert '"%s"' % key in tail
+    assert list(out)[-1] == "summary"

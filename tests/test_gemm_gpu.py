@@ -118,10 +118,10 @@ def test_fprop_full_size_4096x18432x7168(f):
     status_ok()
     mi, ni = sample_points(4096, 18432, seed=3)
     hqx, hsx, hqw, hsw = to_np(qx), to_np(sx), to_np(qw), to_np(sw)
-    # the operands themselves are bit-exact (checked on sampled rows)
-    rows = np.unique(mi)[:64]
-    oq, os_ = oracle.quantize_act_rows(host_bits(X[torch.from_numpy(rows).cuda()]))
-    assert np.array_equal(hqx[rows], oq) and np.array_equal(hsx[:, rows], os_)
+    # the operands themselves are bit-exact: every row of X (codes and scale
+    # bits); W is compared in full in test_quantize_full_gpu.py
+    oq, os_ = oracle.quantize_act_rows(host_bits(X))
+    assert np.array_equal(hqx, oq) and np.array_equal(hsx.view(np.uint32), os_.view(np.uint32))
     ex, ab, _ = oracle.gemm_points(hqx, hsx, hqw, hsw, mi, ni)
     check_gemm(gemm_out_to_f64(C)[mi, ni], ex, ab, True, "fprop full size")
 
@@ -153,6 +153,51 @@ def test_dgrad_with_transposed_weight(f):
     check_gemm(gemm_out_to_f64(C), ex, ab, False, "dgrad")
     ref = (dY.double() @ W.double()).cpu().numpy()
     assert np.abs(gemm_out_to_f64(C) - ref).max() < 0.15 * np.abs(ref).max()
+
+
+def test_dgrad_full_size_4096x7168x18432(f):
+    # dX = dY . W, the third Linear GEMM in FP8 (dssusan.co.kr page, the
+    # Figure 6 passage): dY BF16 4096x18432 (N(0,1e-6), 0.5% x50) in 1x128
+    # groups over the 18432 output features; W the Fprop weight BF16
+    # 18432x7168, whose transposed 128x128-block codes [7168][18432] and
+    # scales [56][144] are the B operand.  M 4096, N 7168, K 18432, BF16 out.
+    dY = synth.matrix(5, 1, 4096, 18432, 1e-3, entry_frac=5e-3, entry_scale=50.0, device="cuda")
+    _, W = synth.fprop_inputs(device="cuda", M=128)
+    qdy, sdy, _, _ = f.quantize_act(dY)
+    _, _, qwt, swt = f.quantize_weight(W, transposed=True)
+    del W
+    C = f.gemm(qdy, sdy, qwt, swt, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    status_ok()
+    mi, ni = sample_points(4096, 7168, seed=6)
+    ex, ab, _ = oracle.gemm_points(to_np(qdy), to_np(sdy), to_np(qwt), to_np(swt), mi, ni)
+    check_gemm(gemm_out_to_f64(C)[mi, ni], ex, ab, True, "dgrad full size")
+
+
+def test_tensor_core_partials_vs_pages_order():
+    # Diagnostic of the tensor core's internal accumulation: the GPU result
+    # (FP32 out, K = 7168 = 56 promotions) against the oracle's literal FP32
+    # procedure of the pages (P_kb rounded to FP32, times fl32(sA*sB), added
+    # in K-block order; "Eliminate Deepseek Ai News For Good", the
+    # MMA-precision passage).  Both approximate the exact sum; if the tensor
+    # core's 128-term partials were exact FP32 the two would differ only by
+    # the promotion's FMA against separate roundings, about 56 ulps of the
+    # running sum.  The bound 2e-5 * sum|ab| is 100x tighter than the parity
+    # tolerance; the measured maximum is printed.
+    import fine_grained_fp8_quantize_b300 as f
+    rng = np.random.default_rng(7168)
+    M, N, K = 256, 512, 7168
+    Aq, Bq = rand_codes(rng, (M, K)), rand_codes(rng, (N, K))
+    sA = rand_scales(rng, (K // 128, M))
+    sB = rand_scales(rng, (N // 128, K // 128))
+    C = run_dense(f, Aq, sA, Bq, sB, torch.float32)
+    ex, ab, pg = oracle.gemm(Aq, sA, Bq, sB)
+    d_pages = float((np.abs(C - pg.astype(np.float64)) / ab).max())
+    d_exact = float((np.abs(C - ex) / ab).max())
+    p_exact = float((np.abs(pg.astype(np.float64) - ex) / ab).max())
+    print("max |C_gpu - C_pages|/sum|ab| = %.3g; |C_gpu - exact| %.3g; |C_pages - exact| %.3g"
+          % (d_pages, d_exact, p_exact))
+    assert d_pages <= 2e-5, d_pages
 
 
 # ----------------------------------------------------------------- grouped
