@@ -242,11 +242,11 @@ int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cu
 
 // One CTA per SM (persistent).  A stream-K launch is cooperative: its CTAs
 // wait on each other's partial tiles, so they must all be resident at once.
-template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK>
+template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK, bool kRing>
 int launch_gemm_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
                   cudaStream_t s) {
-  auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped, kStreamK>;
-  const uint32_t smem = kGrouped ? kSmemGrouped : kSmemDense;
+  auto kern = gemm_kernel<kOutF32, kSbGran, kGrouped, kStreamK, kRing>;
+  const uint32_t smem = gemm_smem_bytes(kSbGran, kGrouped);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return FP8Q_ERR_CUDA;
@@ -264,14 +264,23 @@ int launch_gemm_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMa
   return launch_status();
 }
 
+// Scales go through the shared-memory ring for per-column B scales, the
+// grouped form and long K (more than 64 K-blocks, where the promotion warps'
+// own loads one K-block ahead measured slower); a dense short-K GEMM loads
+// them in the promotion warps (measured faster there).
 template <bool kOutF32, int kSbGran, bool kGrouped>
 int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
                   cudaStream_t s) {
-  if constexpr (kGrouped) {
-    return launch_gemm_k<kOutF32, kSbGran, true, false>(ta, tb, tc, a, grid, s);
+  if constexpr (kGrouped || kSbGran == 1) {
+    return a.streamk ? launch_gemm_k<kOutF32, kSbGran, kGrouped, !kGrouped, true>(ta, tb, tc, a, grid, s)
+                     : launch_gemm_k<kOutF32, kSbGran, kGrouped, false, true>(ta, tb, tc, a, grid, s);
   } else {
-    return a.streamk ? launch_gemm_k<kOutF32, kSbGran, false, true>(ta, tb, tc, a, grid, s)
-                     : launch_gemm_k<kOutF32, kSbGran, false, false>(ta, tb, tc, a, grid, s);
+    const bool ring = a.K / kBK > 64;
+    if (a.streamk)
+      return ring ? launch_gemm_k<kOutF32, kSbGran, false, true, true>(ta, tb, tc, a, grid, s)
+                  : launch_gemm_k<kOutF32, kSbGran, false, true, false>(ta, tb, tc, a, grid, s);
+    return ring ? launch_gemm_k<kOutF32, kSbGran, false, false, true>(ta, tb, tc, a, grid, s)
+                : launch_gemm_k<kOutF32, kSbGran, false, false, false>(ta, tb, tc, a, grid, s);
   }
 }
 
@@ -332,6 +341,7 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   a.E = grouped ? E : 1;
   a.streamk = 0;
   a.sk_tile0 = 0;
+  a.sa_bulk = (M % 4 == 0) ? 1 : 0;  // lds_a == M; sA itself is 16-byte aligned (checked above)
   a.ws = nullptr;
   a.flags = nullptr;
   a.epoch = 0;

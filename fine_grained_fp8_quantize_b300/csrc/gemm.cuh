@@ -54,21 +54,37 @@ constexpr uint32_t kBBytes = kBN * kBK;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
 
-constexpr int kSbRing = 8;                // per-column B-scale slices in flight
-constexpr uint32_t kSbSlotBytes = kBN * 4;  // one K-block's scales of a 256-column tile
+// Scale ring.  A dedicated warp copies every K-block's scales into shared
+// memory ahead of use: the A scales of rows a0 .. a0+131 (a0 = the tile's
+// first row rounded down to a multiple of 4, so one bulk copy starts
+// 16-byte aligned), then the B scales (the two 128x128-block scales of the
+// tile's column halves, or its 256 per-column scales).  Slots hold a batch
+// of consecutive K-blocks, so the promotion warps wait for a slot and
+// release it once per batch and otherwise read plain shared memory.
+constexpr uint32_t kScRowBytes = 132 * 4 + 16;
+__host__ __device__ constexpr uint32_t sc_kb_bytes(int sb_gran) { return kScRowBytes + (sb_gran == 1 ? kBN * 4 : 16); }
+__host__ __device__ constexpr int sc_batch(int sb_gran) { return sb_gran == 1 ? 4 : 8; }
+__host__ __device__ constexpr int sc_ring(int sb_gran, bool grouped) { return sb_gran == 1 ? 2 : (grouped ? 2 : 4); }
+__host__ __device__ constexpr uint32_t sc_slot_bytes(int sb_gran) { return sc_batch(sb_gran) * sc_kb_bytes(sb_gran); }
 
 // dynamic shared memory layout (offsets from a 1024-aligned base)
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-constexpr uint32_t kChunkBytes = 32 * 32;      // epilogue chunk: 32 rows x 32 bytes
-constexpr uint32_t kOffSB = kOffB + kStages * kBBytes;        // per-column sB ring
-constexpr uint32_t kOffStage = kOffSB + kSbRing * kSbSlotBytes;  // epilogue staging, 2 chunks per warp
-constexpr uint32_t kOffBar = kOffStage + 8 * 2 * kChunkBytes;  // 34 mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 48 * 8;               // tmem base, abort flag
-constexpr uint32_t kOffPref = kOffMisc + 16;                  // grouped: tile prefix [E+1]
-constexpr uint32_t kOffRowOff = kOffPref + 4 * (kMaxExperts + 1);  // grouped: row offsets [E+1]
-constexpr uint32_t kSmemDense = kOffPref + 1024;              // + alignment slack
-constexpr uint32_t kSmemGrouped = kOffRowOff + 4 * (kMaxExperts + 1) + 1024;
+constexpr uint32_t kChunkBytes = 32 * 32;                // epilogue chunk: 32 rows x 32 bytes
+constexpr uint32_t kOffSc = kOffB + kStages * kBBytes;  // scale ring
+__host__ __device__ constexpr uint32_t off_stage(int g, bool grp) {  // epilogue staging, 2 chunks per warp
+  return kOffSc + sc_ring(g, grp) * sc_slot_bytes(g);
+}
+__host__ __device__ constexpr uint32_t off_bar(int g, bool grp) { return off_stage(g, grp) + 8 * 2 * kChunkBytes; }
+__host__ __device__ constexpr uint32_t off_misc(int g, bool grp) { return off_bar(g, grp) + 48 * 8; }  // tmem base, abort
+__host__ __device__ constexpr uint32_t off_pref(int g, bool grp) { return off_misc(g, grp) + 16; }  // grouped: [E+1]
+__host__ __device__ constexpr uint32_t off_rowoff(int g, bool grp) { return off_pref(g, grp) + 4 * (kMaxExperts + 1); }
+__host__ __device__ constexpr uint32_t gemm_smem_bytes(int g, bool grp) {
+  return (grp ? off_rowoff(g, grp) + 4 * (kMaxExperts + 1) : off_pref(g, grp)) + 1024;  // + alignment slack
+}
+static_assert(gemm_smem_bytes(128, false) <= 232448 && gemm_smem_bytes(128, true) <= 232448 &&
+                  gemm_smem_bytes(1, false) <= 232448,
+              "GEMM shared memory over the 227 KB per-CTA limit");
 
 struct GemmArgs {
   const float* sA;   // [K/128][lds_a]
@@ -91,6 +107,9 @@ struct GemmArgs {
   // = CTA index) once their flags carry this call's epoch.
   int streamk;
   int sk_tile0;
+  // 1 when every K-block's A scales can be fetched with one bulk copy
+  // (lds_a and M multiples of 4); else the scale warp's lanes copy them
+  int sa_bulk;
   float4* ws;        // [gridDim.x][2 halves][32 column quads][128 rows] float4
   uint32_t* flags;   // [gridDim.x], zero between calls
   uint32_t epoch;    // nonzero, distinct from the previous call's
@@ -180,24 +199,31 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs& a, const in
   return ti;
 }
 
-template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK>
+// kRing: scales through the shared-memory ring (required for per-column B
+// scales and the grouped form); else loaded by the promotion warps.
+template <bool kOutF32, int kSbGran, bool kGrouped, bool kStreamK, bool kRing>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + kOffBar;            // [kStages]
+  constexpr int kScB = sc_batch(kSbGran);              // K-blocks per scale slot
+  constexpr int kScR = sc_ring(kSbGran, kGrouped);     // scale slots
+  constexpr uint32_t kScKb = sc_kb_bytes(kSbGran);
+  constexpr uint32_t kScSlot = sc_slot_bytes(kSbGran);
+  constexpr uint32_t kOffStage = off_stage(kSbGran, kGrouped);
+  const uint32_t bar_full = sbase + off_bar(kSbGran, kGrouped);  // [kStages]
   const uint32_t bar_empty = bar_full + kStages * 8;    // [kStages]
   const uint32_t bar_tfull = bar_empty + kStages * 8;   // [2]
   const uint32_t bar_tempty = bar_tfull + 2 * 8;        // [2]
   const uint32_t bar_drain = bar_tempty + 2 * 8;        // [1]
-  const uint32_t bar_sfull = bar_drain + 8;             // [kSbRing]
-  const uint32_t bar_sempty = bar_sfull + kSbRing * 8;  // [kSbRing]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* pref = reinterpret_cast<int*>(smem + kOffPref);
-  int* roff = reinterpret_cast<int*>(smem + kOffRowOff);
+  const uint32_t bar_sfull = bar_drain + 8;             // [kScR]
+  const uint32_t bar_sempty = bar_sfull + kScR * 8;     // [kScR]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + off_misc(kSbGran, kGrouped));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_misc(kSbGran, kGrouped) + 4);
+  int* pref = reinterpret_cast<int*>(smem + off_pref(kSbGran, kGrouped));
+  int* roff = reinterpret_cast<int*>(smem + off_rowoff(kSbGran, kGrouped));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -213,8 +239,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(bar_tempty + 8 * b, 8);  // one arrive per promotion warp
     }
     mbar_init(bar_drain, 1);
-    for (int r = 0; r < kSbRing; ++r) {
-      mbar_init(bar_sfull + 8 * r, 1);
+    for (int r = 0; r < kScR; ++r) {
+      mbar_init(bar_sfull + 8 * r, 1);   // the scale warp's arrival at the end of a batch (+ its copies' bytes)
       mbar_init(bar_sempty + 8 * r, 8);  // one arrive per promotion warp
     }
     *abort_flag = 0;
@@ -273,26 +299,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // the whole warp runs the loop; one elected lane issues the copies
     {
       uint32_t stage = 0, phase = 0, issued = 0;
-      uint32_t g = 0;  // K-blocks issued so far: position in the sB ring
       bool ok = true;
       // K-blocks [kb_lo, kb_hi) of tile t
       auto load_tile = [&](int t, int64_t kb_lo, int64_t kb_hi) {
         const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
-        // per-column B scales of this tile's columns (the tail tile of an N
-        // that is not a multiple of 256 has 128 columns)
-        const uint32_t sb_bytes = static_cast<uint32_t>(args.N - ti.n0 < kBN ? args.N - ti.n0 : kBN) * 4u;
         for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait_warp(bar_empty + 8 * stage, phase ^ 1u, abort_flag)) { ok = false; break; }
-          if constexpr (kSbGran == 1) {
-            const uint32_t slot = g % kSbRing, sph = (g / kSbRing) & 1u;
-            if (!mbar_wait_warp(bar_sempty + 8 * slot, sph ^ 1u, abort_flag)) { ok = false; break; }
-            if (elect_one()) {
-              mbar_arrive_expect_tx(bar_sfull + 8 * slot, sb_bytes);
-              bulk_load(sbase + kOffSB + slot * kSbSlotBytes, args.sB + kb * args.N + ti.n0, sb_bytes,
-                        bar_sfull + 8 * slot);
-            }
-            __syncwarp();
-          }
           if (elect_one()) {
             mbar_arrive_expect_tx(bar_full + 8 * stage, kABytes + kBBytes);
             tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, static_cast<int32_t>(kb * kBK),
@@ -302,7 +314,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           __syncwarp();
           ++issued;
-          ++g;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       };
@@ -318,13 +329,108 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(bar_full + 8 * stage, phase) && globaltimer_ns() - t0 < 1000000ull) {}
         }
+      }
+    }
+  } else if (kRing && warp == 2) {
+    // ------------------------------------------------------------ scale warp
+    // Fills the scale ring batch by batch, as far ahead as it has free slots
+    // (a slot is free once the promotion warps have read its last K-block),
+    // independently of the operand stages: the scales' global-load latency
+    // hides behind many K-blocks.  Per K-block, A's row scales are one bulk
+    // copy when aligned (else the lanes copy them); the two block scales of
+    // B come from registers the warp loaded once per tile (lanes 0 and 1
+    // store them); per-column B scales are a second bulk copy.  The slot's
+    // full barrier gets the bytes of each copy (expect_tx) and one arrival
+    // at the end of the batch.
+    {
+      uint32_t g = 0;  // K-blocks filled so far: g / kScB is the batch, g % kScB the entry in it
+      bool ok = true;
+      auto fill_tile = [&](int t, int64_t kb_lo, int64_t kb_hi) {
+        const TileInfo ti = tile_info<kGrouped>(t, args, pref, roff);
+        const int64_t a0 = ti.m0 & ~int64_t(3);
+        const int64_t rend = ti.m0 + kBM < args.M ? ti.m0 + kBM : args.M;  // rows of this tile: [m0, rend)
+        // rows a0 .. rend rounded up to 4 (inside the tensor when M % 4 == 0)
+        const uint32_t abytes = static_cast<uint32_t>((rend - a0 + 3) & ~int64_t(3)) * 4u;
+        uint32_t sb_bytes = 0;
         if constexpr (kSbGran == 1) {
-          for (uint32_t i = 0; i < kSbRing && i < g; ++i) {
-            const uint32_t u = g - 1 - i;
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar_sfull + 8 * (u % kSbRing), (u / kSbRing) & 1u) &&
-                   globaltimer_ns() - t0 < 1000000ull) {}
+          // the tail tile of an N that is not a multiple of 256 has 128 columns
+          sb_bytes = static_cast<uint32_t>(args.N - ti.n0 < kBN ? args.N - ti.n0 : kBN) * 4u;
+        }
+        // 128x128-block B scales of the two column halves: lane l holds
+        // those of K-blocks sb_kb0 + l and sb_kb0 + 32 + l (reloaded every
+        // 64 K-blocks)
+        float sbv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        int64_t sb_kb0 = kb_lo;
+        auto load_sb = [&](int64_t kb0) {
+          sb_kb0 = kb0;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int64_t nb = (ti.n0 >> 7) + hh;
+            const bool v = nb * 128 < args.N;
+            const float* row_p = args.sB + ti.sb_off + nb * KB;
+            sbv[hh][0] = v && kb0 + lane < KB ? __ldg(row_p + kb0 + lane) : 0.f;
+            sbv[hh][1] = v && kb0 + 32 + lane < KB ? __ldg(row_p + kb0 + 32 + lane) : 0.f;
           }
+        };
+        if constexpr (kSbGran == 128) load_sb(kb_lo);
+        for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
+          const uint32_t bidx = g / kScB, j = g % kScB;
+          const uint32_t slot = bidx % kScR;
+          const uint32_t sfull = bar_sfull + 8 * slot;
+          if (j == 0 && !mbar_wait_warp(bar_sempty + 8 * slot, ((bidx / kScR) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + kOffSc + slot * kScSlot + j * kScKb;
+          if constexpr (kSbGran == 128) {
+            if (kb - sb_kb0 >= 64) load_sb(kb);
+            const int d = static_cast<int>(kb - sb_kb0);
+            const float b0 = __shfl_sync(0xffffffffu, d < 32 ? sbv[0][0] : sbv[0][1], d & 31);
+            const float b1 = __shfl_sync(0xffffffffu, d < 32 ? sbv[1][0] : sbv[1][1], d & 31);
+            if (lane < 2) reinterpret_cast<float*>(dst + kScRowBytes)[lane] = lane == 0 ? b0 : b1;
+          }
+          if (args.sa_bulk) {
+            if (elect_one()) {
+              mbar_expect_tx(sfull, abytes + sb_bytes);
+              bulk_load(smem_u32(dst), args.sA + kb * args.lds_a + a0, abytes, sfull);
+              if constexpr (kSbGran == 1)
+                bulk_load(smem_u32(dst) + kScRowBytes, args.sB + kb * args.N + ti.n0, sb_bytes, sfull);
+            }
+          } else {
+            float* d4 = reinterpret_cast<float*>(dst);
+            for (int r = lane; r < 132; r += 32) {
+              const int64_t m = a0 + r;
+              d4[r] = m < args.M ? __ldg(args.sA + kb * args.lds_a + m) : 0.f;
+            }
+            if constexpr (kSbGran == 1) {
+              if (elect_one()) {
+                mbar_expect_tx(sfull, sb_bytes);
+                bulk_load(smem_u32(dst) + kScRowBytes, args.sB + kb * args.N + ti.n0, sb_bytes, sfull);
+              }
+            }
+          }
+          __syncwarp();
+          ++g;
+          if (g % kScB == 0 && elect_one()) mbar_arrive(sfull);  // the batch is complete
+          __syncwarp();
+        }
+      };
+      for_each_segment<kStreamK>(args, num_tiles, KB, [&](int t, int64_t lo, int64_t hi) {
+        fill_tile(t, lo, hi);
+        return ok;
+      });
+      // close the last batch if it is open (the CTA's last batch may be
+      // partial, or a failed wait may have left one half filled)
+      if (g % kScB != 0 && elect_one()) mbar_arrive(bar_sfull + 8 * ((g / kScB) % kScR));
+      __syncwarp();
+      if (!ok && lane == 0 && g > 0) {
+        // drain: the copies of the last batches land (bounded) before the
+        // CTA exits; the promotion warps consumed every batch otherwise
+        const uint32_t last = (g - 1) / kScB;
+        for (uint32_t i = 0; i < static_cast<uint32_t>(kScR) && i <= last; ++i) {
+          const uint32_t u = last - i;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar_sfull + 8 * (u % kScR), (u / kScR) & 1u) && globaltimer_ns() - t0 < 1000000ull) {}
         }
       }
     }
@@ -375,10 +481,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;  // tile-local row
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
     uint32_t buf = 0, bphase = 0;
-    uint32_t g = 0;  // K-blocks consumed so far: position in the sB ring
+    uint32_t g = 0;  // K-blocks consumed so far: position in the scale ring
     bool ok = true;
-    const float* __restrict__ sA = args.sA;
-    const float* __restrict__ sB = args.sB;
     // K-blocks [kb_lo, kb_hi) of tile t: promotion, then the epilogue (whole
     // tile, or the stream-K partial exchange)
     auto tile_work = [&](int t, int64_t kb_lo, int64_t kb_hi) {
@@ -387,30 +491,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = m < ti.row_end;
       const int64_t nh = ti.n0 + h * 128;  // first column of this thread's half
       const bool cols_ok = nh < args.N;
-      const float* sb_col = sB + ti.sb_off + (nh >> 7) * KB;  // 128x128 scales of this half, by kb
+      const int a_off = static_cast<int>(ti.m0 & 3);  // the scale slot starts at row m0 rounded down to 4
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
 
-      // scales are loaded one K-block ahead so their latency hides behind
-      // the current block's promotion
-      float sa_next = row_ok ? __ldg(sA + kb_lo * args.lds_a + m) : 0.f;
-      float sb_next = 0.f;
-      if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col + kb_lo) : 0.f;
+      // Scales come either from the scale ring (kRing: a slot entry per
+      // K-block, the slot's full barrier waited on at a batch's first entry,
+      // a 128x128-block slot released once its last entry is read, a
+      // per-column slot only after that K-block's FMAs) or straight from
+      // global memory, loaded one K-block ahead (short K: the scales stay in
+      // L2 and the load returns within a K-block).
+      const float* sb_col = args.sB + ti.sb_off + (nh >> 7) * KB;  // 128x128 scales of this half, by kb
+      float sa_next = 0.f, sb_next = 0.f;
+      if constexpr (!kRing) {
+        sa_next = row_ok ? __ldg(args.sA + kb_lo * args.lds_a + m) : 0.f;
+        sb_next = cols_ok ? __ldg(sb_col + kb_lo) : 0.f;
+      }
 
       for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
-        const float sa = sa_next;
-        const float sb = sb_next;
-        if (kb + 1 < kb_hi) {
-          sa_next = row_ok ? __ldg(sA + (kb + 1) * args.lds_a + m) : 0.f;
-          if constexpr (kSbGran == 128) sb_next = cols_ok ? __ldg(sb_col + kb + 1) : 0.f;
-        }
-        const float4* sbs = nullptr;  // per-column B scales of this half (smem)
-        uint32_t slot = 0;
-        if constexpr (kSbGran == 1) {
-          slot = g % kSbRing;
-          if (!mbar_wait_warp(bar_sfull + 8 * slot, (g / kSbRing) & 1u, abort_flag)) { ok = false; break; }
-          sbs = reinterpret_cast<const float4*>(smem + kOffSB + slot * kSbSlotBytes) + h * 32;
+        float sa, sb = 0.f;
+        const float4* sbs = nullptr;  // per-column B scales of this half
+        if constexpr (kRing) {
+          const uint32_t bidx = g / kScB, jb = g % kScB;
+          const uint32_t slot = bidx % kScR;
+          if (jb == 0 && !mbar_wait_warp(bar_sfull + 8 * slot, (bidx / kScR) & 1u, abort_flag)) { ok = false; break; }
+          const uint8_t* ent = smem + kOffSc + slot * kScSlot + jb * kScKb;
+          sa = reinterpret_cast<const float*>(ent)[row + a_off];
+          if constexpr (kSbGran == 128) {
+            sb = reinterpret_cast<const float*>(ent + kScRowBytes)[h];
+            if (jb == kScB - 1) {  // the batch's last entry is in registers: the slot is free
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_sempty + 8 * slot);
+            }
+          } else {
+            sbs = reinterpret_cast<const float4*>(ent + kScRowBytes) + h * 32;
+          }
+        } else {
+          sa = sa_next;
+          sb = sb_next;
+          if (kb + 1 < kb_hi) {
+            sa_next = row_ok ? __ldg(args.sA + (kb + 1) * args.lds_a + m) : 0.f;
+            sb_next = cols_ok ? __ldg(sb_col + kb + 1) : 0.f;
+          }
         }
         if (!mbar_wait_warp(bar_tfull + 8 * buf, bphase, abort_flag)) { ok = false; break; }
         __syncwarp();
@@ -448,8 +571,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if constexpr (kSbGran == 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_sempty + 8 * slot);
+          if (g % kScB == kScB - 1) {  // this K-block was its slot's last: the slot is free
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sempty + 8 * ((g / kScB) % kScR));
+          }
         }
         ++g;
         buf ^= 1u;
