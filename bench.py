@@ -624,11 +624,15 @@ def case_moe(args, f, torch, synth, pk, iters):
     counts = off[1:] - off[:-1]
     active = [int(e) for e in np.flatnonzero(counts)]
     E, Nn, Kk = MOE["E"], MOE["N"], MOE["H"]
-    Xm, Wm = synth.moe_inputs(device="cuda", experts=active)
-    qw, sw = f.quantize_weight(Wm.view(E * Nn, Kk))
-    del Wm
-    qw = qw.view(E, Nn, Kk)
-    sw = sw.view(E, Nn // 128, Kk // 128)
+    # tokens N(0,1); each active expert's weight drawn and quantized in turn
+    # (the same values moe_inputs gives), so only the codes stay resident
+    Xm = synth.matrix(4, 1, MOE["T"], Kk, 1.0, device="cuda")
+    qw = torch.zeros(E, Nn, Kk, dtype=torch.uint8, device="cuda")
+    sw = torch.ones(E, Nn // 128, Kk // 128, dtype=torch.float32, device="cuda")
+    for e in active:
+        f.fp8q_quantize_weight(synth.matrix(4, 1000 + e, Nn, Kk, 0.02, device="cuda"), qw[e], sw[e])
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     src_d = torch.from_numpy(src.astype(np.int32)).cuda()
     off_d = torch.from_numpy(off.astype(np.int32)).cuda()
     R = len(src)

@@ -25,9 +25,9 @@
 //                K-block it tcgen05.ld's its slice of the partial, frees the
 //                buffer, and does acc = fma(P, sA*sB, acc).  At the end of
 //                a tile it rounds (BF16, RNE) or keeps FP32 and stores.
-// Registers: warpgroup 0 gives up all but 56 per thread
-// (setmaxnreg) so the two promotion warpgroups can hold 224 each: the
-// 384 x 168 registers of the launch are exactly 128 x 56 + 256 x 224.
+// Registers: warpgroup 0 gives up all but 56 (ring variants: 40) per
+// thread (setmaxnreg) so the two promotion warpgroups can hold 224 (232)
+// each: the 384 x 168 registers of the launch, exactly.
 // The grid is persistent (one CTA per SM); tiles are striped over CTAs.
 // Every mbarrier wait is bounded (see mbar_wait): on expiry the kernel
 // records a timeout in the status word and unwinds without trapping.
@@ -46,8 +46,16 @@ constexpr int kBN = 256;
 constexpr int kBK = 128;
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 384;
-constexpr uint32_t kRegsCtl = 56;    // warpgroup 0 after setmaxnreg.dec
-constexpr uint32_t kRegsMath = 224;  // warpgroups 1-2 after setmaxnreg.inc
+// Register split after setmaxnreg, warpgroup 0 (producer, MMA issuer, scale
+// warp, one idle warp) / warpgroups 1-2 (promotion).  Both add up to the
+// launch's 384 x 168 (128 x ctl + 256 x math; setmaxnreg.inc may not ask for
+// more).  The ring variants keep more state in the promotion warps and give
+// them 232; the others measured best at 56 / 224.
+__host__ __device__ constexpr uint32_t regs_ctl(bool ring) { return ring ? 40u : 56u; }
+__host__ __device__ constexpr uint32_t regs_math(bool ring) { return ring ? 232u : 224u; }
+static_assert(128 * regs_ctl(false) + 256 * regs_math(false) <= 384 * 168 &&
+                  128 * regs_ctl(true) + 256 * regs_math(true) <= 384 * 168,
+              "register split over the launch's 384 x 168");
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kABytes = kBM * kBK;  // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK;  // 32 KB
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_tiles = kGrouped ? pref[args.E] : args.tiles_m * args.tiles_n;
 
   if (warp < 4) {
-    setmaxnreg_dec<kRegsCtl>();
+    setmaxnreg_dec<regs_ctl(kRing)>();
   }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -475,7 +483,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ promotion
-    setmaxnreg_inc<kRegsMath>();
+    setmaxnreg_inc<regs_math(kRing)>();
     const int q = warp & 3;         // TMEM lane quadrant this warp may access
     const int h = (warp - 4) >> 2;  // column half of the tile: 0 or 1
     const int row = q * 32 + lane;  // tile-local row
