@@ -69,10 +69,14 @@ constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kBN);
 // tile's column halves, or its 256 per-column scales).  Slots hold a batch
 // of consecutive K-blocks, so the promotion warps wait for a slot and
 // release it once per batch and otherwise read plain shared memory.
+// A slot is refilled (kScR - 1) batches before it is read: per-column
+// entries are large (1.5 KB a K-block), so they come two K-blocks a batch
+// in four slots, which measured faster than four in two slots (less lead)
+// and one in eight (a barrier round per K-block).
 constexpr uint32_t kScRowBytes = 132 * 4 + 16;
 __host__ __device__ constexpr uint32_t sc_kb_bytes(int sb_gran) { return kScRowBytes + (sb_gran == 1 ? kBN * 4 : 16); }
-__host__ __device__ constexpr int sc_batch(int sb_gran) { return sb_gran == 1 ? 4 : 8; }
-__host__ __device__ constexpr int sc_ring(int sb_gran, bool grouped) { return sb_gran == 1 ? 2 : (grouped ? 2 : 4); }
+__host__ __device__ constexpr int sc_batch(int sb_gran) { return sb_gran == 1 ? 2 : 8; }
+__host__ __device__ constexpr int sc_ring(int sb_gran, bool grouped) { return sb_gran == 1 ? 4 : (grouped ? 2 : 4); }
 __host__ __device__ constexpr uint32_t sc_slot_bytes(int sb_gran) { return sc_batch(sb_gran) * sc_kb_bytes(sb_gran); }
 
 // dynamic shared memory layout (offsets from a 1024-aligned base)
