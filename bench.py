@@ -474,7 +474,7 @@ def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
         "roofline": tensor_roofline("gemm_kernel<bf16 out, 128x128 B scales>", flops, tg.mean_ms(), pk,
                                     "fprop_4096x18432x7168", sustained=ms >= 500.0),
         "step_kernels": {
-            "quant_x_rows_4096x7168": hbm_roofline("quant_rows_kernel<bf16>", xbytes, tx.mean_ms(), pk,
+            "quant_x_rows_4096x7168": hbm_roofline("quant_rc_kernel<bf16, row>", xbytes, tx.mean_ms(), pk,
                                                    "x_rows_4096x7168"),
             "quant_w_blocks_18432x7168": hbm_roofline("quant_pipe_kernel<blk>", wbytes, tw.mean_ms(), pk,
                                                       "w_blocks_18432x7168")},
@@ -584,8 +584,8 @@ def case_wgrad(args, f, torch, synth, pk, iters):
             "step_ms": round(ms_all, 4), "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
             "roofline": tensor_roofline("gemm_kernel<f32 out, per-column B scales, stream-K>", fl, ms_g, pk,
                                         "wgrad_2048x7168x8192", note=False),
-            "quant_cols_dY_8192x2048": hbm_roofline("quant_pipe_kernel<col>", qb_dy, ms_qdy, pk, "cols_8192x2048"),
-            "quant_cols_X_8192x7168": hbm_roofline("quant_pipe_kernel<col>", qb_x, ms_qx, pk, "cols_8192x7168")}
+            "quant_cols_dY_8192x2048": hbm_roofline("quant_rc_kernel<bf16, col>", qb_dy, ms_qdy, pk, "cols_8192x2048"),
+            "quant_cols_X_8192x7168": hbm_roofline("quant_rc_kernel<bf16, col>", qb_x, ms_qx, pk, "cols_8192x7168")}
 
 
 def case_dgrad(args, f, torch, synth, pk, iters):
@@ -614,7 +614,7 @@ def case_dgrad(args, f, torch, synth, pk, iters):
             "step_TFLOP/s": round(fl / ms_all / 1e9, 1),
             "roofline": tensor_roofline("gemm_kernel<bf16 out, 128x128 B scales>", fl, ms_g, pk,
                                         "dgrad_4096x7168x18432", note=False),
-            "quant_w_transposed_18432x7168": hbm_roofline("quant_pipe_kernel<blkT>", wtbytes, ms_wt, pk,
+            "quant_w_transposed_18432x7168": hbm_roofline("quant_rc_kernel<bf16, blkT>", wtbytes, ms_wt, pk,
                                                           "w_blocksT_18432x7168")}
 
 

@@ -161,10 +161,10 @@ int launch_quant_pipe(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   return launch_status();
 }
 
-// BF16 row and/or transposed column groups: the split-role persistent kernel
-// (one 128-thread warpgroup per path), as many CTAs as fit on the device
-// (occupancy probed once per device).
-template <bool kRow, bool kCol>
+// BF16 through the split-role persistent kernel (one 128-thread warpgroup
+// per output), as many CTAs as fit on the device (occupancy probed once per
+// device).
+template <bool kRow, bool kCol, bool kBlk>
 int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   static std::atomic<int> resident[64];
   DeviceInfo di;
@@ -172,7 +172,7 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
   const int st = check_device(&di);
   if (st != FP8Q_OK) return st;
-  auto kern = quant_rc_kernel<kRow, kCol>;
+  auto kern = quant_rc_kernel<kRow, kCol, kBlk>;
   constexpr int kSmem = rc_smem_bytes(kRow, kCol);
   constexpr int kThreads = (kRow ? 128 : 0) + (kCol ? 128 : 0);
   int per_sm = resident[dev].load(std::memory_order_relaxed);
@@ -189,9 +189,11 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   std::memset(&tm_col, 0, sizeof(tm_col));
   if (!make_tmap_bf16_tile(&tm_x, a.x, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)))
     return FP8Q_ERR_CUDA;
-  if (kRow && !make_tmap_u8(&tm_row, a.q_row, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M), 128))
+  if (kRow && !make_tmap_u8(&tm_row, kBlk ? a.q_blk : a.q_row, static_cast<uint64_t>(a.K),
+                            static_cast<uint64_t>(a.M), 128))
     return FP8Q_ERR_CUDA;
-  if (kCol && !make_tmap_u8(&tm_col, a.q_colT, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), 128))
+  if (kCol && !make_tmap_u8(&tm_col, kBlk ? a.q_blkT : a.q_colT, static_cast<uint64_t>(a.M),
+                            static_cast<uint64_t>(a.K), 128))
     return FP8Q_ERR_CUDA;
   const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
@@ -199,43 +201,21 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   return launch_status();
 }
 
-// BF16 rows only (and the row gather): one warp per 16-row slab, as many
-// CTAs as fit on the device at once (occupancy probed once per device).
-int launch_quant_rows(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
-  static std::atomic<int> resident[64];
-  DeviceInfo di;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
-  const int st = check_device(&di);
-  if (st != FP8Q_OK) return st;
-  int per_sm = resident[dev].load(std::memory_order_relaxed);
-  if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_rows_kernel, kRowsThreads, 0) != cudaSuccess)
-      return FP8Q_ERR_CUDA;
-    if (per_sm < 1) per_sm = 1;
-    resident[dev].store(per_sm, std::memory_order_relaxed);
-  }
-  const int64_t slabs = tiles * 8;
-  const int64_t need = (slabs + kRowsThreads / 32 - 1) / (kRowsThreads / 32);
-  const int64_t cap = static_cast<int64_t>(di.sms) * per_sm;
-  const int grid = static_cast<int>(need < cap ? need : cap);
-  quant_rows_kernel<<<grid, kRowsThreads, 0, stream>>>(a, slabs);
-  return launch_status();
-}
-
-// FP32 input: one CTA per tile.  BF16 rows + transposed columns: the
-// split-role kernel (both paths busy).  BF16 rows only, not gathered: one warp
-// per 16-row slab.  Other BF16 modes (the row gather, columns only, 128x128
-// blocks): the pipelined kernel, which keeps 12 warps per SM where a one-path
-// split-role CTA would keep 8 (measured faster).
+// FP32 input: one CTA per tile.  BF16: the TMA-fed split-role kernel, one
+// warpgroup per output (rows, transposed columns, blocks with their
+// transpose, or either alone), except for the row gather (scattered rows:
+// the pipelined kernel's one bulk copy per row) and 128x128 blocks without
+// the transpose, where the pipelined kernel's 12 warps per SM measured
+// faster than one warpgroup per CTA (5.72 vs 5.48 TB/s on 18432 x 7168).
 template <int kMode>
 int launch_quant_dt(int in_dtype, const QuantArgs& a, int64_t gx, int64_t gy, cudaStream_t s) {
   if (in_dtype == FP8Q_FP32) return launch_quant<true, kMode>(a, gx, gy, s);
-  if constexpr (kMode == (kQRow | kQCol)) return launch_quant_rc<true, true>(a, gx * gy, s);
+  if constexpr (kMode == (kQRow | kQCol)) return launch_quant_rc<true, true, false>(a, gx * gy, s);
+  if constexpr (kMode == kQCol) return launch_quant_rc<false, true, false>(a, gx * gy, s);
+  if constexpr (kMode == (kQBlk | kQBlkT)) return launch_quant_rc<true, true, true>(a, gx * gy, s);
+  if constexpr (kMode == kQBlkT) return launch_quant_rc<false, true, true>(a, gx * gy, s);
   if constexpr (kMode == kQRow) {
-    // gathered rows come scattered: the pipelined kernel's one bulk copy per
-    // row measured faster there (160 vs 180 us for 65,536 of 16,384 rows)
-    if (a.src_rows == nullptr) return launch_quant_rows(a, gx * gy, s);
+    if (a.src_rows == nullptr) return launch_quant_rc<true, false, false>(a, gx * gy, s);
   }
   return launch_quant_pipe<kMode>(a, gx * gy, s);
 }

@@ -366,15 +366,20 @@ __global__ void __launch_bounds__(128, quant_pipe_min_blocks(kMode))
 }
 
 // ---------------------------------------------------------------------------
-// Rows + transposed columns of BF16 activations in one pass, split by role.
-// Persistent, 256 threads, two 128 x 128 tiles in flight per CTA, each
-// arriving as one dense TMA box (128 rows x 256 bytes).
-//   warps 0-3  row path: thread r owns tile row r (16 x 16-byte reads, in a
-//              rotated order that keeps them free of bank conflicts); its
-//              1x128 amax is a packed BF16 max over the row (no shuffles).
-//   warps 4-7  column path: thread (p, h) owns columns 2p, 2p+1 over the
-//              64 rows of half h (64 x 4-byte reads); the two halves meet in
-//              shared memory for the 128x1 amax.
+// BF16 tiles through TMA, split by role: row groups and/or transposed column
+// groups of activations, or (kBlk) a 128x128 block's codes as-is and/or
+// transposed.  Persistent, 128 threads per path present, two 128 x 128 tiles
+// in flight per CTA, each arriving as one dense TMA box (128 rows x 256 bytes).
+//   row path     thread r owns tile row r (16 x 16-byte reads, in a rotated
+//                order that keeps them free of bank conflicts); its 1x128
+//                amax is a packed BF16 max over the row (no shuffles).
+//   column path  thread (p, h) owns columns 2p, 2p+1 over the 64 rows of
+//                half h (64 x 4-byte reads); the two halves meet in shared
+//                memory for the 128x1 amax.
+// In block mode each path holds the whole tile, so each finds the block's
+// amax by itself (warp shuffles, then its 4 warps' maxima in shared memory)
+// and casts with that one scale: the row path writes the codes as they lie,
+// the column path their transpose.
 // Each path writes its 128 x 128 codes into a staged shared-memory tile in
 // the 128-byte-swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8),
 // which keeps those writes conflict-free) and one thread stores the tile
@@ -398,7 +403,7 @@ constexpr int rc_smem_bytes(bool row, bool col) {
 }
 static_assert(kRcTileBytes % 1024 == 0 && kRcCodeBytes % 1024 == 0, "staged tiles must stay 1024-aligned");
 
-template <bool kRow, bool kCol>
+template <bool kRow, bool kCol, bool kBlk>
 __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     quant_rc_kernel(const QuantArgs args, int64_t num_tiles, const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_row, const __grid_constant__ CUtensorMap tm_col) {
@@ -406,6 +411,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   // [2][128][kRcPitch] inputs, then the staged code tiles
   uint8_t* rsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~uintptr_t(1023));
   __shared__ float s_cmax[2][128];                 // column maxima of each 64-row half
+  __shared__ float s_bmax[2][4];                   // block mode: per-warp maxima of each path
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ int abort_word;
   volatile int* abort_flag = &abort_word;
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   // Input tile tt: one TMA load of 128 rows x 128 columns (256-byte rows,
   // dense, no swizzle).  The row path reads its row's 16-byte chunks in a
   // rotated order, which keeps those reads free of bank conflicts.
-  static_assert(kCol, "the TMA-fed rows+columns kernel needs column groups (M % 128 == 0, no row gather)");
+  static_assert(kRow || kCol, "at least one path");
   auto tile_bytes = [&](int64_t) -> uint32_t { return static_cast<uint32_t>(kRcTileBytes); };
   auto issue_tile = [&](int64_t tt, int b) {  // one thread
     tma_load_2d(buf0 + b * kRcTileBytes, &tm_x, static_cast<int32_t>((tt % kbt) * 128),
@@ -509,9 +515,22 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
 #pragma unroll
       for (int i = 1; i < 64; ++i) mx = __hmax2(mx, __habs2(bf2_of(w[i])));
       const uint32_t mw = u32_of(mx);
+      float amax = fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw));
+      if constexpr (kBlk) {
+        // the 128x128 block's amax: over the warp, then over the path's 4 warps
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((tid & 31) == 0) s_bmax[0][tid >> 5] = amax;
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        amax = fmaxf(fmaxf(s_bmax[0][0], s_bmax[0][1]), fmaxf(s_bmax[0][2], s_bmax[0][3]));
+      }
       float sc, inv;
-      group_scale(fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw)), sc, inv);
-      if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
+      group_scale(amax, sc, inv);
+      if constexpr (kBlk) {
+        if (tid == 0) args.s_blk[mb * kbt + kb] = sc;
+      } else {
+        if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
+      }
       uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);  // row tid
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
@@ -536,13 +555,27 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
 #pragma unroll
       for (int r = 1; r < 64; ++r) mx = __hmax2(mx, __habs2(bf2_of(w[r])));
       const uint32_t mw = u32_of(mx);
-      s_cmax[hh][2 * p] = bf16lo_to_f32(mw);
-      s_cmax[hh][2 * p + 1] = bf16hi_to_f32(mw);
-      asm volatile("bar.sync 2, 128;" ::: "memory");
       float sc0, inv0, sc1, inv1;
-      group_scale(fmaxf(s_cmax[0][2 * p], s_cmax[1][2 * p]), sc0, inv0);
-      group_scale(fmaxf(s_cmax[0][2 * p + 1], s_cmax[1][2 * p + 1]), sc1, inv1);
-      if (hh == 0) *reinterpret_cast<float2*>(args.s_col + mb * K + k0 + 2 * p) = make_float2(sc0, sc1);
+      if constexpr (kBlk) {
+        // the 128x128 block's amax: over the warp, then over the path's 4 warps
+        float amax = fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((ctid & 31) == 0) s_bmax[1][ctid >> 5] = amax;
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        amax = fmaxf(fmaxf(s_bmax[1][0], s_bmax[1][1]), fmaxf(s_bmax[1][2], s_bmax[1][3]));
+        group_scale(amax, sc0, inv0);
+        sc1 = sc0;
+        inv1 = inv0;
+        if (ctid == 0) args.s_blkT[kb * (M >> 7) + mb] = sc0;
+      } else {
+        s_cmax[hh][2 * p] = bf16lo_to_f32(mw);
+        s_cmax[hh][2 * p + 1] = bf16hi_to_f32(mw);
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        group_scale(fmaxf(s_cmax[0][2 * p], s_cmax[1][2 * p]), sc0, inv0);
+        group_scale(fmaxf(s_cmax[0][2 * p + 1], s_cmax[1][2 * p + 1]), sc1, inv1);
+        if (hh == 0) *reinterpret_cast<float2*>(args.s_col + mb * K + k0 + 2 * p) = make_float2(sc0, sc1);
+      }
       // staged transposed tile: row = column of x, 128 token bytes per row
       uint8_t* ct = rsm + 2 * kRcTileBytes + (kRow ? kRcCodeBytes : 0);
       uint4* d0 = reinterpret_cast<uint4*>(ct + (2 * p) * kRcCodePitch);
@@ -583,70 +616,5 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   }
 }
 
-
-// ---------------------------------------------------------------------------
-// quant_rows_kernel: BF16 input, 1x128 row groups only (it supports the row
-// gather; the library routes gathered rows to quant_pipe_kernel, faster there).  The work unit is a slab of 16 rows x 128 columns, one warp
-// per slab, slabs striped over all warps of a persistent grid; warps never
-// wait for each other.  Per step a warp reads two rows (lanes 0-15 the first,
-// 16-31 the second), each lane 8 consecutive values with one 16-byte load, so
-// a row's amax is a packed BF16 max (exact) and four shuffles among its 16
-// lanes.  All eight steps' loads are in flight before any arithmetic.  Codes
-// leave as 8-byte stores (a half-warp writes one 128-byte row segment); each
-// row's scale is one 4-byte store.  The scale and cast are those of
-// quant_tile_body, so the codes are the same bit for bit.
-// ---------------------------------------------------------------------------
-constexpr int kRowsThreads = 256;
-
-__global__ void __launch_bounds__(kRowsThreads) quant_rows_kernel(const QuantArgs args, int64_t num_slabs) {
-  const int lane = threadIdx.x & 31;
-  const int64_t K = args.K;
-  const int64_t M = args.M;
-  const int64_t KT = K >> 7;
-  const int half = lane >> 4;  // which of the two rows of a step
-  const int col8 = lane & 15;  // 8-column slot within the row
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsThreads / 32);
-  for (int64_t sl = static_cast<int64_t>(blockIdx.x) * (kRowsThreads / 32) + (threadIdx.x >> 5); sl < num_slabs;
-       sl += warps) {
-    const int64_t t = sl >> 3;
-    const int w = static_cast<int>(sl & 7);  // rows 16w .. 16w+15 of the tile
-    const int64_t rt = t / KT;
-    const int64_t kt = t - rt * KT;
-    const int64_t col = kt * 128 + col8 * 8;
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t m = rt * 128 + w * 16 + 2 * i + half;
-      if (m < M) {
-        const int64_t src = (args.src_rows != nullptr) ? static_cast<int64_t>(__ldg(args.src_rows + m)) : m;
-        v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(args.x) + src * K + col));
-      } else {
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t m = rt * 128 + w * 16 + 2 * i + half;
-      const uint4 u = v[i];
-      const __nv_bfloat162 a2 = __hmax2(__hmax2(__habs2(bf2_of(u.x)), __habs2(bf2_of(u.y))),
-                                        __hmax2(__habs2(bf2_of(u.z)), __habs2(bf2_of(u.w))));
-      const uint32_t ab = u32_of(a2);
-      float amax = fmaxf(bf16lo_to_f32(ab), bf16hi_to_f32(ab));
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      float sc, inv;
-      group_scale(amax, sc, inv);
-      if (m < M) {
-        const uint2 c = make_uint2(
-            cvt_e4m3x4(bf16lo_to_f32(u.x) * inv, bf16hi_to_f32(u.x) * inv, bf16lo_to_f32(u.y) * inv,
-                       bf16hi_to_f32(u.y) * inv),
-            cvt_e4m3x4(bf16lo_to_f32(u.z) * inv, bf16hi_to_f32(u.z) * inv, bf16lo_to_f32(u.w) * inv,
-                       bf16hi_to_f32(u.w) * inv));
-        *reinterpret_cast<uint2*>(args.q_row + m * K + col) = c;
-        if (col8 == 0) args.s_row[kt * args.ld_srow + m] = sc;
-      }
-    }
-  }
-}
 
 }  // namespace fp8q

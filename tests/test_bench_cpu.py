@@ -93,7 +93,7 @@ def test_reference_arm_prints_the_contract_line():
 
 def test_summary_is_compact_and_last():
     r = bench.tensor_roofline("gemm_kernel<x>", 1.5e12, 1.0, PK, "no_such_workload")
-    q = bench.hbm_roofline("quant_rows_kernel<x>", 3.0e9, 1.0, PK, "no_such_workload")
+    q = bench.hbm_roofline("quant_rc_kernel<x>", 3.0e9, 1.0, PK, "no_such_workload")
     out = {"value": 1.0, "roofline": r, "step_kernels": {"quant_x_rows_4096x7168": q},
            "breakdown": {"act_quant_16384x7168": {"roofline": q},
                          "wgrad_2048x7168x8192": {"roofline": r, "quant_cols_dY_8192x2048": q,
