@@ -317,6 +317,13 @@ int gemm_common(const uint8_t* Aq, const float* sA, const uint8_t* Bq, const flo
   a.K = K;
   a.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
   a.tiles_n = static_cast<int>((N + kBN - 1) / kBN);
+  // Raster order.  Concurrent CTAs walk K in step, so a wave reads the A rows
+  // of all its M-tiles once; when A is too large to stay in L2 from one wave
+  // to the next (K = 18432 Dgrad: 75 MB of codes, re-read by each of 6 waves)
+  // tiles go in groups of 16 M-tiles over all N-tiles, which halves the A
+  // rows a wave touches (measured 1.6% faster there, same elsewhere).
+  constexpr int kMGroup = 16;
+  a.m_group = (M * K > (int64_t(64) << 20) && a.tiles_m > kMGroup) ? kMGroup : a.tiles_m;
   a.row_offsets = row_offsets;
   a.E = grouped ? E : 1;
   a.streamk = 0;

@@ -108,6 +108,7 @@ struct GemmArgs {
   int64_t K;
   int tiles_m;       // dense
   int tiles_n;
+  int m_group;       // dense: M-tiles per raster group (tiles_m: plain M-fastest order)
   const int32_t* row_offsets;  // grouped [E+1]
   int E;
   // stream-K (dense only, kernel variant kStreamK): tiles below sk_tile0 are
@@ -182,8 +183,14 @@ template <bool kGrouped>
 __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs& a, const int* pref, const int* roff) {
   TileInfo ti;
   if constexpr (!kGrouped) {
-    const int mt = t % a.tiles_m;
-    const int nt = t / a.tiles_m;
+    // groups of m_group M-tiles, each over all N-tiles, M-fastest inside
+    const int per = a.m_group * a.tiles_n;
+    const int grp = t / per;
+    const int w = t - grp * per;
+    const int m_lo = grp * a.m_group;
+    const int gm = a.tiles_m - m_lo < a.m_group ? a.tiles_m - m_lo : a.m_group;
+    const int mt = m_lo + w % gm;
+    const int nt = w / gm;
     ti.m0 = static_cast<int64_t>(mt) * kBM;
     ti.row_end = a.M;
     ti.n0 = static_cast<int64_t>(nt) * kBN;

@@ -174,6 +174,25 @@ def test_dgrad_full_size_4096x7168x18432(f):
     check_gemm(gemm_out_to_f64(C)[mi, ni], ex, ab, True, "dgrad full size")
 
 
+def test_raster_groups_with_ragged_last_group(f):
+    # A larger than 64 MiB of codes switches the dense GEMM to its grouped
+    # tile order (16 M-tiles per group over all N-tiles).  M 2240 = 17.5
+    # M-tiles: groups of 16 and 2, the last M-tile ragged; N 384: one full
+    # and one half N-tile; K 30720 (240 K-blocks).  Random codes (no NaN) and
+    # scales 2^U(-10,3); every output of one row per M-tile and one column
+    # per N-tile is compared with the oracle.
+    rng = np.random.default_rng(2240)
+    M, N, K = 2240, 384, 30720
+    assert M * K > 64 << 20
+    Aq, Bq = rand_codes(rng, (M, K)), rand_codes(rng, (N, K))
+    sA = rand_scales(rng, (K // 128, M))
+    sB = rand_scales(rng, ((N + 127) // 128, K // 128))
+    C = run_dense(f, Aq, sA, Bq, sB, torch.bfloat16)
+    mi, ni = sample_points(M, N, seed=11)
+    ex, ab, _ = oracle.gemm_points(Aq, sA, Bq, sB, mi, ni)
+    check_gemm(C[mi, ni], ex, ab, True, "grouped raster order")
+
+
 def test_tensor_core_partials_vs_pages_order():
     # Diagnostic of the tensor core's internal accumulation: the GPU result
     # (FP32 out, K = 7168 = 56 promotions) against the oracle's literal FP32
