@@ -167,11 +167,15 @@ def test_dgrad_full_size_4096x7168x18432(f):
     _, _, qwt, swt = f.quantize_weight(W, transposed=True)
     del W
     C = f.gemm(qdy, sdy, qwt, swt, out_dtype=torch.bfloat16)
+    # 896 tiles = 6.05 waves: with a workspace the tail goes through stream-K
+    # (the scale-ring variant with split tiles)
+    Cs = f.gemm(qdy, sdy, qwt, swt, out_dtype=torch.bfloat16, workspace=f.gemm_workspace())
     torch.cuda.synchronize()
     status_ok()
     mi, ni = sample_points(4096, 7168, seed=6)
     ex, ab, _ = oracle.gemm_points(to_np(qdy), to_np(sdy), to_np(qwt), to_np(swt), mi, ni)
     check_gemm(gemm_out_to_f64(C)[mi, ni], ex, ab, True, "dgrad full size")
+    check_gemm(gemm_out_to_f64(Cs)[mi, ni], ex, ab, True, "dgrad full size, stream-K")
 
 
 def test_raster_groups_with_ragged_last_group(f):
