@@ -245,9 +245,9 @@ int launch_gemm_k(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMa
 }
 
 // Scales go through the shared-memory ring for per-column B scales, the
-// grouped form and long K (more than 64 K-blocks, where the promotion warps'
-// own loads one K-block ahead measured slower); a dense short-K GEMM loads
-// them in the promotion warps (measured faster there).
+// grouped form, stream-K and long K (more than 64 K-blocks: 2187 against 1907
+// TFLOP/s at K = 18432); a dense short-K data-parallel GEMM loads them in the
+// promotion warps (2468 against 2357 TFLOP/s at K = 7168).
 template <bool kOutF32, int kSbGran, bool kGrouped>
 int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& a, int grid,
                   cudaStream_t s) {
@@ -256,9 +256,9 @@ int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMa
                      : launch_gemm_k<kOutF32, kSbGran, kGrouped, false, true>(ta, tb, tc, a, grid, s);
   } else {
     const bool ring = a.K / kBK > 64;
-    if (a.streamk)
-      return ring ? launch_gemm_k<kOutF32, kSbGran, false, true, true>(ta, tb, tc, a, grid, s)
-                  : launch_gemm_k<kOutF32, kSbGran, false, true, false>(ta, tb, tc, a, grid, s);
+    // stream-K always takes the scale ring: the variant with per-thread
+    // scale loads spills there (4096x7168x7168: 17% slower)
+    if (a.streamk) return launch_gemm_k<kOutF32, kSbGran, false, true, true>(ta, tb, tc, a, grid, s);
     return ring ? launch_gemm_k<kOutF32, kSbGran, false, false, true>(ta, tb, tc, a, grid, s)
                 : launch_gemm_k<kOutF32, kSbGran, false, false, false>(ta, tb, tc, a, grid, s);
   }
