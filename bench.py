@@ -447,14 +447,18 @@ def gpu_fprop(args, rank, world, dist, f, torch, synth, pk):
     tx = Timed(torch, args.steps)
     tw = Timed(torch, args.steps)
 
+    # W is quantized first: the kernel that follows the previous step's GEMM
+    # shares the memory bus with the write-back of its 151 MB of output, and
+    # the larger, bandwidth-bound W pass absorbs that better than the short X
+    # pass (step 0.75% faster than X first)
     def step(timed):
         if timed:
-            tx(stream, lambda: f.fp8q_quantize_act(X, qx, sx))
             tw(stream, lambda: f.fp8q_quantize_weight(W, qw, sw))
+            tx(stream, lambda: f.fp8q_quantize_act(X, qx, sx))
             tg(stream, lambda: f.fp8q_gemm(qx, sx, qw, sw, Y))
         else:
-            f.fp8q_quantize_act(X, qx, sx)
             f.fp8q_quantize_weight(W, qw, sw)
+            f.fp8q_quantize_act(X, qx, sx)
             f.fp8q_gemm(qx, sx, qw, sw, Y)
 
     ms, clocks = run_timed(torch, stream, step, args.steps, args.warmup, dist)
