@@ -85,14 +85,39 @@ def peaks():
         return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
 
 
+def _strip_comments(src):
+    """C/C++ source without // and /* */ comments and blank lines (string
+    literals are left alone), so that editing a comment keeps the hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_sha():
-    """Hash of the CUDA sources: a recorded ncu traffic figure is used only
-    while the kernels are the ones it was taken of."""
+    """Hash of the CUDA sources' code (comments stripped): a recorded ncu
+    traffic figure is used only while the kernels are the ones it was taken
+    of."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fine_grained_fp8_quantize_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

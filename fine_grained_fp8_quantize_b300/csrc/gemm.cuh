@@ -20,6 +20,9 @@
 //                MMAs of block kb+1 overlap the promotion of block kb.
 //                Warps 0 and 1 run their loops as whole warps and issue from
 //                one elected lane, which keeps the operands warp-uniform.
+//   warp 2       scale warp (variants with the scale ring): copies each
+//                K-block's A and B scales into a shared-memory ring ahead of
+//                use, a batch of K-blocks per slot (see the ring below).
 //   warps 4..11  promotion + epilogue: each thread owns one row and 128
 //                columns of the 128x256 tile in 128 FP32 registers; per
 //                K-block it tcgen05.ld's its slice of the partial, frees the
@@ -28,7 +31,9 @@
 // Registers: warpgroup 0 gives up all but 56 (ring variants: 40) per
 // thread (setmaxnreg) so the two promotion warpgroups can hold 224 (232)
 // each: the 384 x 168 registers of the launch, exactly.
-// The grid is persistent (one CTA per SM); tiles are striped over CTAs.
+// The grid is persistent (one CTA per SM); tiles are striped over CTAs,
+// M-tile fastest (in groups of M-tiles when A is large), and a stream-K
+// variant splits the last waves' tiles by K over all CTAs.
 // Every mbarrier wait is bounded (see mbar_wait): on expiry the kernel
 // records a timeout in the status word and unwinds without trapping.
 #pragma once
