@@ -107,3 +107,13 @@ def test_summary_is_compact_and_last():
                 "quant_cols_dY", "quant_cols_X"):
         assert '"%s"' % key in tail
     assert list(out)[-1] == "summary"
+
+
+def test_kernel_hash_ignores_comments_only():
+    import bench
+    a = bench._strip_comments('int a = 1;  // note\n/* block\n comment */\nconst char* s = "x // y";\n')
+    b = bench._strip_comments('int a = 1;\nconst char* s = "x // y";  /* other */\n')
+    c = bench._strip_comments('int a = 2;\nconst char* s = "x // y";\n')
+    assert a == b
+    assert a != c
+    assert '"x // y"' in a
