@@ -794,7 +794,7 @@ def case_mx(args, f, torch, synth, pk, iters):
                                         note=False),
             "act_quant_16384x7168": {
                 "ms": round(ms_q, 4), "GB/s": round(qbytes / (ms_q * 1e-3) / 1e9, 1), "bytes": qbytes,
-                "roofline": hbm_roofline("quant_mx_kernel<bf16>", qbytes, ms_q, pk, "mx_act_16384x7168")}}
+                "roofline": hbm_roofline("quant_rc_kernel<bf16, mx>", qbytes, ms_q, pk, "mx_act_16384x7168")}}
 
 
 def case_ceiling(args, f, torch, synth, pk, iters):

@@ -164,7 +164,7 @@ int launch_quant_pipe(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
 // BF16 through the split-role persistent kernel (one 128-thread warpgroup
 // per output), as many CTAs as fit on the device (occupancy probed once per
 // device).
-template <bool kRow, bool kCol, bool kBlk>
+template <bool kRow, bool kCol, bool kBlk, bool kMx = false>
 int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   static std::atomic<int> resident[64];
   DeviceInfo di;
@@ -172,7 +172,7 @@ int launch_quant_rc(const QuantArgs& a, int64_t tiles, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
   const int st = check_device(&di);
   if (st != FP8Q_OK) return st;
-  auto kern = quant_rc_kernel<kRow, kCol, kBlk>;
+  auto kern = quant_rc_kernel<kRow, kCol, kBlk, kMx>;
   constexpr int kSmem = rc_smem_bytes(kRow, kCol);
   constexpr int kThreads = (kRow ? 128 : 0) + (kCol ? 128 : 0);
   int per_sm = resident[dev].load(std::memory_order_relaxed);
@@ -670,8 +670,17 @@ int fp8q_mx_quantize(const void* x, int in_dtype, int64_t rows, int64_t K, uint8
   if (!x || !q || !s) return FP8Q_ERR_NULL;
   if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return FP8Q_ERR_ALIGN;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  return in_dtype == FP8Q_FP32 ? launch_quant_mx<true>(x, rows, K, q, s, cs)
-                               : launch_quant_mx<false>(x, rows, K, q, s, cs);
+  if (in_dtype == FP8Q_FP32) return launch_quant_mx<true>(x, rows, K, q, s, cs);
+  // BF16: the TMA-fed split-role kernel's row path in MX mode
+  const int st = check_device(nullptr);
+  if (st != FP8Q_OK) return st;
+  QuantArgs a{};
+  a.x = x;
+  a.M = rows;
+  a.K = K;
+  a.q_row = q;
+  a.s_mx = s;
+  return launch_quant_rc<true, false, false, true>(a, (K / 128) * ((rows + 127) / 128), cs);
 }
 
 int fp8q_mx_gemm(const uint8_t* Aq, const uint8_t* sA, const uint8_t* Bq, const uint8_t* sB, void* C, int64_t M,

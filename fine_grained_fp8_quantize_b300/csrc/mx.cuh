@@ -33,7 +33,8 @@
 namespace fp8q {
 
 // ---------------------------------------------------------------------------
-// Quantizer: 1x32 groups along K, E8M0 scales
+// Quantizer: 1x32 groups along K, E8M0 scales (FP32 input; BF16 input runs
+// the TMA-fed quant_rc_kernel in its MX mode, same arithmetic)
 // ---------------------------------------------------------------------------
 // Work unit: a slab of 16 rows x 128 columns (one eighth of a 128 x 128
 // tile), one warp per slab, slabs striped over all warps of a persistent

@@ -24,6 +24,7 @@
 
 #include <cstdint>
 
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace fp8q {
@@ -49,6 +50,7 @@ struct QuantArgs {
   float* s_blk;
   uint8_t* q_blkT;
   float* s_blkT;
+  uint8_t* s_mx;            // MX row mode: E8M0 scales in the tensor core's tiled layout
 };
 
 // 16 rows x 8 columns of the input held by one thread.
@@ -403,7 +405,7 @@ constexpr int rc_smem_bytes(bool row, bool col) {
 }
 static_assert(kRcTileBytes % 1024 == 0 && kRcCodeBytes % 1024 == 0, "staged tiles must stay 1024-aligned");
 
-template <bool kRow, bool kCol, bool kBlk>
+template <bool kRow, bool kCol, bool kBlk, bool kMx = false>
 __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     quant_rc_kernel(const QuantArgs args, int64_t num_tiles, const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_row, const __grid_constant__ CUtensorMap tm_col) {
@@ -427,6 +429,7 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
   // dense, no swizzle).  The row path reads its row's 16-byte chunks in a
   // rotated order, which keeps those reads free of bank conflicts.
   static_assert(kRow || kCol, "at least one path");
+  static_assert(!kMx || (kRow && !kCol && !kBlk), "MX groups: the row path alone");
   auto tile_bytes = [&](int64_t) -> uint32_t { return static_cast<uint32_t>(kRcTileBytes); };
   auto issue_tile = [&](int64_t tt, int b) {  // one thread
     tma_load_2d(buf0 + b * kRcTileBytes, &tm_x, static_cast<int32_t>((tt % kbt) * 128),
@@ -509,45 +512,95 @@ __global__ void __launch_bounds__((kRow ? 128 : 0) + (kCol ? 128 : 0), 2)
     if (tid == 0 && tn < num_tiles) issue_tile(tn, b);
 
     if (row_role) {
-      // ---- 1x128 row group of row m
       const int64_t m = m0 + tid;
-      __nv_bfloat162 mx = __habs2(bf2_of(w[0]));
+      if constexpr (kMx) {
+        // ---- MX: four 1x32 groups of row m.  Slot k holds code chunk
+        // j = (k + tid) % 8 (16 columns), which belongs to group j / 2.
+        float gmax[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = __hmax2(mx, __habs2(bf2_of(w[i])));
-      const uint32_t mw = u32_of(mx);
-      float amax = fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw));
-      if constexpr (kBlk) {
-        // the 128x128 block's amax: over the warp, then over the path's 4 warps
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 h = __habs2(bf2_of(w[8 * k]));
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if ((tid & 31) == 0) s_bmax[0][tid >> 5] = amax;
-        asm volatile("bar.sync 3, 128;" ::: "memory");
-        amax = fmaxf(fmaxf(s_bmax[0][0], s_bmax[0][1]), fmaxf(s_bmax[0][2], s_bmax[0][3]));
-      }
-      float sc, inv;
-      group_scale(amax, sc, inv);
-      if constexpr (kBlk) {
-        if (tid == 0) args.s_blk[mb * kbt + kb] = sc;
-      } else {
-        if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
-      }
-      uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);  // row tid
+          for (int i = 1; i < 8; ++i) h = __hmax2(h, __habs2(bf2_of(w[8 * k + i])));
+          const uint32_t hw = u32_of(h);
+          const float a = fmaxf(bf16lo_to_f32(hw), bf16hi_to_f32(hw));
+          const int g = ((k + tid) & 7) >> 1;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        uint32_t c[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t a = w[4 * i + 2 * u], bb = w[4 * i + 2 * u + 1];
-          c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
-                            bf16hi_to_f32(bb) * inv);
+          for (int gg = 0; gg < 4; ++gg) gmax[gg] = g == gg ? fmaxf(gmax[gg], a) : gmax[gg];
         }
-        st[(((i >> 1) + tid) & 7) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);  // code chunk of slot i/2
-      }
-      fence_proxy_async_smem();
-      asm volatile("bar.sync 3, 128;" ::: "memory");
-      if (tid == 0) {
-        tma_store_2d(&tm_row, smem_u32(rsm + 2 * kRcTileBytes), static_cast<int32_t>(k0), static_cast<int32_t>(m0));
-        bulk_commit();
+        uint32_t word = 0;
+        float ginv[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t byte = mx_scale_byte(gmax[g]);
+          ginv[g] = __uint_as_float((254u - byte) << 23);  // 2^-(byte - 127), a normal float
+          word |= byte << (8 * g);
+        }
+        // rows past the end get scale 1 (byte 127): defined, never read into C
+        const int64_t rt_count = (M + 127) >> 7;
+        *reinterpret_cast<uint32_t*>(args.s_mx + (kb * rt_count + mb) * 512 + (tid & 31) * 16 + (tid >> 5) * 4) =
+            m < M ? word : 0x7F7F7F7Fu;
+        uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);  // row tid
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int g = ((k + tid) & 7) >> 1;
+          const float inv = g == 0 ? ginv[0] : g == 1 ? ginv[1] : g == 2 ? ginv[2] : ginv[3];
+          uint32_t c[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t a = w[8 * k + 2 * u], bb = w[8 * k + 2 * u + 1];
+            c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
+                              bf16hi_to_f32(bb) * inv);
+          }
+          st[((k + tid) & 7) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);  // code chunk of slot k
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        if (tid == 0) {
+          tma_store_2d(&tm_row, smem_u32(rsm + 2 * kRcTileBytes), static_cast<int32_t>(k0),
+                       static_cast<int32_t>(m0));
+          bulk_commit();
+        }
+      } else {
+        // ---- 1x128 row group of row m
+        __nv_bfloat162 mx = __habs2(bf2_of(w[0]));
+#pragma unroll
+        for (int i = 1; i < 64; ++i) mx = __hmax2(mx, __habs2(bf2_of(w[i])));
+        const uint32_t mw = u32_of(mx);
+        float amax = fmaxf(bf16lo_to_f32(mw), bf16hi_to_f32(mw));
+        if constexpr (kBlk) {
+          // the 128x128 block's amax: over the warp, then over the path's 4 warps
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          if ((tid & 31) == 0) s_bmax[0][tid >> 5] = amax;
+          asm volatile("bar.sync 3, 128;" ::: "memory");
+          amax = fmaxf(fmaxf(s_bmax[0][0], s_bmax[0][1]), fmaxf(s_bmax[0][2], s_bmax[0][3]));
+        }
+        float sc, inv;
+        group_scale(amax, sc, inv);
+        if constexpr (kBlk) {
+          if (tid == 0) args.s_blk[mb * kbt + kb] = sc;
+        } else {
+          if (m < M) args.s_row[kb * args.ld_srow + m] = sc;
+        }
+        uint4* st = reinterpret_cast<uint4*>(rsm + 2 * kRcTileBytes + tid * kRcCodePitch);  // row tid
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          uint32_t c[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t a = w[4 * i + 2 * u], bb = w[4 * i + 2 * u + 1];
+            c[u] = cvt_e4m3x4(bf16lo_to_f32(a) * inv, bf16hi_to_f32(a) * inv, bf16lo_to_f32(bb) * inv,
+                              bf16hi_to_f32(bb) * inv);
+          }
+          st[(((i >> 1) + tid) & 7) ^ (tid & 7)] = make_uint4(c[0], c[1], c[2], c[3]);  // code chunk of slot i/2
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        if (tid == 0) {
+          tma_store_2d(&tm_row, smem_u32(rsm + 2 * kRcTileBytes), static_cast<int32_t>(k0), static_cast<int32_t>(m0));
+          bulk_commit();
+        }
       }
     } else if constexpr (kCol) {
       // ---- 128x1 column groups of columns k0 + 2p, k0 + 2p + 1
