@@ -534,14 +534,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
 
       for (int64_t kb = kb_lo; kb < kb_hi; ++kb) {
-        float sa, sb = 0.f;
-        const float4* sbs = nullptr;  // per-column B scales of this half
+        float sa = 0.f, sb = 0.f;
+        float sa4[4] = {0.f, 0.f, 0.f, 0.f};  // per-column variant: the scales of this thread's four rows
+        const float2* sb2 = nullptr;          // per-column variant: B scales of this half
         if constexpr (kRing) {
           const uint32_t bidx = g / kScB, jb = g % kScB;
           const uint32_t slot = bidx % kScR;
           if (jb == 0 && !mbar_wait_warp(bar_sfull + 8 * slot, (bidx / kScR) & 1u, abort_flag)) { ok = false; break; }
           const uint8_t* ent = smem + kOffSc + slot * kScSlot + jb * kScKb;
-          sa = reinterpret_cast<const float*>(ent)[row + a_off];
+          if constexpr (kSbGran == 1) {
+            // the 16x256b layout: this thread's rows are q*32 + lane/4 + {0, 8, 16, 24}
+            const float* sar = reinterpret_cast<const float*>(ent) + a_off + q * 32 + (lane >> 2);
+            sa4[0] = sar[0];
+            sa4[1] = sar[8];
+            sa4[2] = sar[16];
+            sa4[3] = sar[24];
+          } else {
+            sa = reinterpret_cast<const float*>(ent)[row + a_off];
+          }
           if constexpr (kSbGran == 128) {
             sb = reinterpret_cast<const float*>(ent + kScRowBytes)[h];
             if (jb == kScB - 1) {  // the batch's last entry is in registers: the slot is free
@@ -549,7 +559,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               if (lane == 0) mbar_arrive(bar_sempty + 8 * slot);
             }
           } else {
-            sbs = reinterpret_cast<const float4*>(ent + kScRowBytes) + h * 32;
+            // columns 8j + 2(lane%4) and +1 of this half, j = 0..15: float2 4j + lane%4
+            sb2 = reinterpret_cast<const float2*>(ent + kScRowBytes) + h * 64 + (lane & 3);
           }
         } else {
           sa = sa_next;
@@ -563,35 +574,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         tc_fence_after();
         const uint32_t taddr = tmem_base + t_lane + buf * kBN + h * 128;
-        const float scale = sa * sb;
+        if constexpr (kSbGran == 1) {
+          // Per-column B scales: the partial is read in the 16x256b layout,
+          // where a thread holds 4 rows x 32 columns (pairs), so it needs 32
+          // column scales (16 float2 loads) instead of all 128 of its half.
+          // acc[lb*64 + 4j + k]: row q*32 + lb*16 + lane/4 + 8*(k/2), column
+          // h*128 + 8j + 2(lane%4) + k%2.
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t p[64];
-          tmem_ld_32x32b_x64(taddr + c2 * 64, p);
-          tmem_ld_wait();
-          if (c2 == 1) {
-            // the whole partial of this warp is in registers: free the buffer
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t pa[32], pb[32];
+            tmem_ld_16x256b_x8(taddr + ch * 64, pa);
+            tmem_ld_16x256b_x8(taddr + (16u << 16) + ch * 64, pb);
+            tmem_ld_wait();
+            if (ch == 1) {
+              // the whole partial of this warp is in registers: free the buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+            }
+            // acc += (P * sB) * sA, two columns per packed FP32 instruction
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float* a0 = acc + 4 * (ch * 8 + j);
+              float* a1 = a0 + 64;
+              const float2 bj = sb2[4 * (ch * 8 + j)];
+              float t0, t1, t2, t3;
+              mul2(t0, t1, __uint_as_float(pa[4 * j + 0]), __uint_as_float(pa[4 * j + 1]), bj.x, bj.y);
+              mul2(t2, t3, __uint_as_float(pa[4 * j + 2]), __uint_as_float(pa[4 * j + 3]), bj.x, bj.y);
+              fma2(a0[0], a0[1], t0, t1, sa4[0], sa4[0]);
+              fma2(a0[2], a0[3], t2, t3, sa4[1], sa4[1]);
+              mul2(t0, t1, __uint_as_float(pb[4 * j + 0]), __uint_as_float(pb[4 * j + 1]), bj.x, bj.y);
+              mul2(t2, t3, __uint_as_float(pb[4 * j + 2]), __uint_as_float(pb[4 * j + 3]), bj.x, bj.y);
+              fma2(a1[0], a1[1], t0, t1, sa4[2], sa4[2]);
+              fma2(a1[2], a1[3], t2, t3, sa4[3], sa4[3]);
+            }
           }
-          // acc += P * scale, two columns per packed FP32 instruction
-          if constexpr (kSbGran == 128) {
+        } else {
+          const float scale = sa * sb;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t p[64];
+            tmem_ld_32x32b_x64(taddr + c2 * 64, p);
+            tmem_ld_wait();
+            if (c2 == 1) {
+              // the whole partial of this warp is in registers: free the buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+            }
+            // acc += P * scale, two columns per packed FP32 instruction
 #pragma unroll
             for (int j = 0; j < 64; j += 2)
               fma2(acc[c2 * 64 + j], acc[c2 * 64 + j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), scale,
                    scale);
-          } else {
-#pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 b4 = sbs[c2 * 16 + j4];
-              float* a = acc + c2 * 64 + 4 * j4;
-              float t0, t1, t2, t3;
-              mul2(t0, t1, __uint_as_float(p[4 * j4 + 0]), __uint_as_float(p[4 * j4 + 1]), b4.x, b4.y);
-              mul2(t2, t3, __uint_as_float(p[4 * j4 + 2]), __uint_as_float(p[4 * j4 + 3]), b4.z, b4.w);
-              fma2(a[0], a[1], t0, t1, sa, sa);
-              fma2(a[2], a[3], t2, t3, sa, sa);
-            }
           }
         }
         if constexpr (kSbGran == 1) {
@@ -679,6 +714,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint8_t* cb = stg + (c & 1) * kChunkBytes;
             if (lane == 0) bulk_wait_read<1>();  // the chunk buffer's previous store has read it
             __syncwarp();
+            if constexpr (kSbGran == 1) {
+              // the 16x256b layout (see the promotion): rows lb*16 + lane/4
+              // + 8*hi of the warp's 32, column pairs 2(lane%4) of each
+              // 8-column block
+#pragma unroll
+              for (int lb = 0; lb < 2; ++lb) {
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                  uint8_t* rp = cb + (lb * 16 + (lane >> 2) + 8 * hi) * 32;
+                  const float* a = acc + lb * 64 + 2 * hi;
+                  if constexpr (kOutF32) {
+                    *reinterpret_cast<uint2*>(rp + 8 * (lane & 3)) =
+                        make_uint2(__float_as_uint(a[4 * c]), __float_as_uint(a[4 * c + 1]));
+                  } else {
+                    *reinterpret_cast<uint32_t*>(rp + 4 * (lane & 3)) = cvt_bf16x2(a[8 * c], a[8 * c + 1]);
+                    *reinterpret_cast<uint32_t*>(rp + 16 + 4 * (lane & 3)) = cvt_bf16x2(a[8 * c + 4], a[8 * c + 5]);
+                  }
+                }
+              }
+            } else {
             uint4 v0, v1;
             if constexpr (kOutF32) {
               v0 = make_uint4(__float_as_uint(acc[8 * c + 0]), __float_as_uint(acc[8 * c + 1]),
@@ -695,6 +750,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             *reinterpret_cast<uint4*>(cb + lane * 32) = v0;
             *reinterpret_cast<uint4*>(cb + lane * 32 + 16) = v1;
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -702,7 +758,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               bulk_commit();
             }
           }
-        } else if (row_ok) {
+        } else if (kSbGran != 1 && row_ok) {  // (dense per-column tiles always go through TMA)
           if constexpr (kOutF32) {
             float4* out = reinterpret_cast<float4*>(static_cast<float*>(args.C) + m * args.N + nh);
 #pragma unroll
