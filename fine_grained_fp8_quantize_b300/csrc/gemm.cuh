@@ -89,8 +89,10 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kChunkBytes = 32 * 32;                // epilogue chunk: 32 rows x 32 bytes
 constexpr uint32_t kOffSc = kOffB + kStages * kBBytes;  // scale ring
-__host__ __device__ constexpr uint32_t off_stage(int g, bool grp) {  // epilogue staging, 2 chunks per warp
-  return kOffSc + sc_ring(g, grp) * sc_slot_bytes(g);
+// epilogue staging, 2 chunks per warp: the source of TMA tensor stores, so
+// 128-byte aligned
+__host__ __device__ constexpr uint32_t off_stage(int g, bool grp) {
+  return (kOffSc + sc_ring(g, grp) * sc_slot_bytes(g) + 127u) & ~127u;
 }
 __host__ __device__ constexpr uint32_t off_bar(int g, bool grp) { return off_stage(g, grp) + 8 * 2 * kChunkBytes; }
 __host__ __device__ constexpr uint32_t off_misc(int g, bool grp) { return off_bar(g, grp) + 48 * 8; }  // tmem base, abort
@@ -99,6 +101,11 @@ __host__ __device__ constexpr uint32_t off_rowoff(int g, bool grp) { return off_
 __host__ __device__ constexpr uint32_t gemm_smem_bytes(int g, bool grp) {
   return (grp ? off_rowoff(g, grp) + 4 * (kMaxExperts + 1) : off_pref(g, grp)) + 1024;  // + alignment slack
 }
+static_assert(off_stage(128, false) % 128 == 0 && off_stage(128, true) % 128 == 0 && off_stage(1, false) % 128 == 0,
+              "TMA store sources must be 128-byte aligned");
+static_assert(sc_slot_bytes(128) % 16 == 0 && sc_slot_bytes(1) % 16 == 0 && sc_kb_bytes(128) % 16 == 0 &&
+                  sc_kb_bytes(1) % 16 == 0,
+              "bulk copies into the scale ring need 16-byte aligned destinations");
 static_assert(gemm_smem_bytes(128, false) <= 232448 && gemm_smem_bytes(128, true) <= 232448 &&
                   gemm_smem_bytes(1, false) <= 232448,
               "GEMM shared memory over the 227 KB per-CTA limit");
