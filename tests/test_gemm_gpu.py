@@ -97,15 +97,18 @@ def test_dense_zero_rows_is_noop(f):
     assert C.shape == (0, 128)
 
 
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 1024), (200, 640, 512)])
-def test_wgrad_per_column_scales(f, M, N, K):
+def test_wgrad_per_column_scales(f, M, N, K, out):
+    # every output element; half N-tiles and a ragged M-tile; both output
+    # types (the per-column variant stores from its own register layout)
     rng = np.random.default_rng(N + K)
     Aq, Bq = rand_codes(rng, (M, K)), rand_codes(rng, (N, K))
     sA = rand_scales(rng, (K // 128, M))
     sB = rand_scales(rng, (K // 128, N))
-    C = run_dense(f, Aq, sA, Bq, sB, torch.float32, gran=1)
+    C = run_dense(f, Aq, sA, Bq, sB, out, gran=1)
     ex, ab, _ = oracle.gemm(Aq, sA, Bq, sB, sb_gran=1)
-    check_gemm(C, ex, ab, False, "wgrad")
+    check_gemm(C, ex, ab, out == torch.bfloat16, "wgrad")
 
 
 def test_fprop_full_size_4096x18432x7168(f):
