@@ -324,6 +324,7 @@ def _flags_zero(f, ws):
     (256, 512, 8192, 128, torch.float32),     # 4 tiles, 64 K-blocks each: every tile split ~37 ways
     (1000, 1280, 4096, 128, torch.bfloat16),  # ragged rows, 40 tiles
     (384, 768, 2048, 1, torch.float32),       # per-column B scales
+    (384, 768, 8192, 1, torch.bfloat16),      # per-column B scales split by stream-K (9 tiles, 576 K-blocks)
     (200, 384, 1024, 128, torch.bfloat16),    # N tail tile of 128 columns
 ])
 def test_streamk_matches_oracle(f, workspace, M, N, K, gran, out):
